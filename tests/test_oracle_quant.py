@@ -1,0 +1,140 @@
+"""Pins for the oracle's quantisers (page 4: max-abs taken online per 1x128
+activation tile and per 128x128 weight block; pages 2/3: integral power-of-2
+scales for some activations; page 4: Wgrad runs in FP8, which needs 128x1
+tiles along tokens)."""
+import math
+import os
+
+import numpy as np
+import pytest
+import torch
+
+from fp8_fine_grained_16_b300 import synthetic as S
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden", "worked_tiles_1x128.txt")
+
+
+def _bits(t):
+    return S.bf16_bits(t)
+
+
+def _rand_bf16(shape, seed, scale=1.0):
+    g = torch.Generator().manual_seed(seed)
+    return (torch.randn(shape, generator=g) * scale).to(torch.bfloat16)
+
+
+def _load_golden():
+    tiles = []
+    for line in open(GOLDEN):
+        line = line.strip()
+        if not line or line.startswith("#"):
+            continue
+        f = line.split()
+        if f[0] == "tile":
+            tiles.append(dict(name=f[1], pow2=f[2] == "pow2", scale=float.fromhex(f[3]), xs=[]))
+        else:
+            tiles[-1]["xs"].append((int(f[1]), float.fromhex(f[2]), int(f[3], 16)))
+    return tiles
+
+
+@pytest.mark.parametrize("tile", _load_golden(), ids=lambda t: t["name"] + ("-pow2" if t["pow2"] else ""))
+def test_worked_tiles(orc, tile):
+    x = torch.zeros((1, 128), dtype=torch.float32)
+    for i, v, _ in tile["xs"]:
+        x[0, i] = v
+    xb = x.to(torch.bfloat16)
+    assert torch.equal(xb.float(), x)            # fixture values are bf16-exact
+    q, s = orc.quant_act_1x128(_bits(xb), flags=1 if tile["pow2"] else 0)
+    assert s[0, 0] == np.float32(tile["scale"])
+    expect = np.zeros(128, np.uint8)
+    for i, _, c in tile["xs"]:
+        expect[i] = c
+    assert np.array_equal(q[0], expect)
+
+
+def _decode(orc, q):
+    table = orc.e4m3_decode(np.arange(256))
+    return table[q]
+
+
+@pytest.mark.parametrize("pow2", [False, True])
+def test_amax_maps_to_448(orc, pow2):
+    d = S.tiny_dense()
+    xb = _bits(d["x"])
+    q, s = orc.quant_act_1x128(xb, flags=int(pow2))
+    x = d["x"].float().numpy()
+    v = _decode(orc, q)
+    M, K = x.shape
+    for m in range(M):
+        for kb in range(K // 128):
+            t = x[m, kb * 128:(kb + 1) * 128]
+            qt = v[m, kb * 128:(kb + 1) * 128]
+            i = int(np.argmax(np.abs(t)))
+            if not pow2:
+                assert abs(qt[i]) == 448.0 and math.copysign(1, qt[i]) == math.copysign(1, t[i])
+            else:
+                sc = float(s[kb, m])
+                assert math.frexp(sc)[0] == 0.5                       # exact power of two
+                assert 448.0 * sc >= abs(t[i]) > 224.0 * sc           # smallest such power
+                assert 224.0 <= np.abs(qt).max() <= 448.0
+
+
+@pytest.mark.parametrize("pow2", [False, True])
+def test_dequant_error_bound(orc, pow2):
+    """|x - q*s| <= max(|x| 2^-4, s 2^-10) + |x| 2^-20 for every element."""
+    xt = torch.cat([_rand_bf16((64, 1024), 3), _rand_bf16((64, 1024), 4, 1e-3),
+                    S.dense_linear(M=64, N=128, K=1024)["x"]])
+    q, s = orc.quant_act_1x128(_bits(xt), flags=int(pow2))
+    x = xt.double().numpy()
+    sc = np.repeat(s.T.astype(np.float64), 128, axis=1)
+    err = np.abs(x - _decode(orc, q) * sc)
+    bound = np.maximum(np.abs(x) * 2.0 ** -4, sc * 2.0 ** -10) + np.abs(x) * 2.0 ** -20
+    assert np.all(err <= bound)
+
+
+def test_tile_locality_outlier_columns(orc):
+    """The x100 outlier columns change only the tiles that contain them."""
+    g = torch.Generator().manual_seed(0)
+    base = torch.randn((128, 512), generator=g)
+    out = base.clone()
+    out[:, 5] *= 100
+    out[:, 260] *= 100
+    qa, sa = orc.quant_act_1x128(_bits(base.to(torch.bfloat16)))
+    qb, sb = orc.quant_act_1x128(_bits(out.to(torch.bfloat16)))
+    touched = {0, 2}
+    for kb in range(4):
+        same = np.array_equal(sa[kb], sb[kb]) and np.array_equal(qa[:, kb * 128:(kb + 1) * 128],
+                                                                 qb[:, kb * 128:(kb + 1) * 128])
+        assert same == (kb not in touched)
+
+
+@pytest.mark.parametrize("pow2", [False, True])
+def test_128x1_is_1x128_of_transpose(orc, pow2):
+    x = _rand_bf16((384, 200), 11)
+    qT, s = orc.quant_act_128x1(_bits(x), flags=int(pow2))
+    q2, s2 = orc.quant_act_1x128(_bits(x.t().contiguous()), flags=int(pow2))
+    assert np.array_equal(qT, q2) and np.array_equal(s, s2)
+
+
+@pytest.mark.parametrize("pow2", [False, True])
+def test_weight_block_scale_is_block_amax(orc, pow2):
+    w = _rand_bf16((256, 384), 5, 0.02)
+    w[100, 300] = 3.0
+    q, s = orc.quant_weight_128x128(_bits(w), flags=int(pow2))
+    wf = w.float().numpy()
+    for nb in range(2):
+        for kb in range(3):
+            blk = wf[nb * 128:(nb + 1) * 128, kb * 128:(kb + 1) * 128]
+            want, _ = orc.tile_scale(float(np.abs(blk).max()), int(pow2))
+            assert s[nb, kb] == want
+    # the block holding the 3.0 maps it to 448 in default mode
+    if not pow2:
+        assert q[100, 300] == 0x7E
+
+
+def test_zero_tile_is_finite(orc):
+    x = torch.zeros((2, 256), dtype=torch.bfloat16)
+    x[1, 200] = -1.0
+    q, s = orc.quant_act_1x128(_bits(x))
+    assert np.all(np.isfinite(s)) and s[0, 0] == np.float32(2.0 ** -64 / 448)
+    assert np.all(q[0] == 0) and q[1, 200] == 0xFE
