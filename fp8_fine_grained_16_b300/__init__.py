@@ -8,11 +8,12 @@ loudly if the library has not been built.
 """
 from __future__ import annotations
 
-__all__ = ["fp8bs", "synthetic"]
+import importlib
+
+__all__ = ["fp8bs", "synthetic", "build"]
 
 
 def __getattr__(name):
-    if name.startswith("fp8_") or name in ("fp8bs", "Status", "FP8Error"):
-        from . import fp8bs
-        return fp8bs if name == "fp8bs" else getattr(fp8bs, name)
+    if name.startswith("fp8_") or name == "FP8Error":
+        return getattr(importlib.import_module(__name__ + ".fp8bs"), name)
     raise AttributeError(name)

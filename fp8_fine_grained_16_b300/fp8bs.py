@@ -1,0 +1,249 @@
+"""Thin ctypes binding of libfp8bs.so (declared in include/fp8bs.h).
+
+Every function here has the name of the C entry point it calls and only
+marshals arguments: it checks the torch tensors' dtype, device and layout,
+allocates missing outputs with ``torch.empty`` on the input's device, passes
+raw device pointers plus the current CUDA stream, and raises ``FP8Error`` on
+a non-zero status.  All arithmetic runs in the library's CUDA kernels; there
+is no fallback.  Importing this module fails if the library is not built.
+
+bf16 tensors are ``torch.bfloat16``; E4M3 codes are ``torch.uint8`` (view
+them as ``torch.float8_e4m3fn`` if wanted); scales are ``torch.float32``.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libfp8bs.so")
+
+if not os.path.exists(LIB_PATH):
+    raise ImportError("libfp8bs.so is not built: run `python -m fp8_fine_grained_16_b300.build`")
+
+lib = ctypes.CDLL(LIB_PATH)
+
+FP8_OK = 0
+FP8_SCALE_POW2 = 1
+FP8_BSCALE_BLOCK128 = 0
+FP8_BSCALE_ROW = 1
+FP8_OUT_BF16 = 0
+FP8_OUT_F32 = 1
+FP8_ERR_TIMEOUT = -5
+FP8_ERR_OFFSETS = -6
+
+_P = ctypes.c_void_p
+_I64 = ctypes.c_int64
+_I = ctypes.c_int
+_U32 = ctypes.c_uint32
+
+_SIGS = {
+    "fp8_cast_e4m3": [_P, _I64, _P, _P],
+    "fp8_quant_act_1x128": [_P, _I64, _I64, _I64, _P, _P, _U32, _P],
+    "fp8_quant_act_128x1": [_P, _I64, _I64, _I64, _P, _P, _U32, _P],
+    "fp8_quant_weight_128x128": [_P, _I64, _I64, _I64, _P, _P, _U32, _P],
+    "fp8_gemm_blockscaled": [_P, _P, _P, _P, _I, _P, _I, _I64, _I64, _I64, _P],
+    "fp8_grouped_gemm_blockscaled": [_P, _P, _P, _P, _P, _I, _I64, _I64, _I64, _P, _P],
+    "fp8_moe_route_topk": [_P, _I64, _I, _I, _P, _P, _P, _P, _P, _P, _P],
+    "fp8_permute_rows": [_P, _P, _I64, _I64, _P, _I64, _P, _P, _P],
+    "fp8_moe_combine_bf16": [_P, _I64, _P, _P, _I64, _I, _I64, _P, _P],
+    "fp8_get_status": [_P],
+    "fp8_selftest_wait_timeout": [ctypes.c_uint64, _P],
+}
+for _name, _args in _SIGS.items():
+    _f = getattr(lib, _name)
+    _f.argtypes = _args
+    _f.restype = _I
+lib.fp8_moe_route_workspace_size.argtypes = [_I64, _I]
+lib.fp8_moe_route_workspace_size.restype = _I64
+lib.fp8_strerror.argtypes = [_I]
+lib.fp8_strerror.restype = ctypes.c_char_p
+lib.fp8_version.argtypes = []
+lib.fp8_version.restype = _I
+
+#: every symbol include/fp8bs.h declares
+EXPORTED = sorted(list(_SIGS) + ["fp8_moe_route_workspace_size", "fp8_strerror", "fp8_version"])
+
+
+class FP8Error(RuntimeError):
+    def __init__(self, fn: str, code: int):
+        super().__init__("%s failed: %s (%d)" % (fn, lib.fp8_strerror(code).decode(), code))
+        self.code = code
+
+
+def _check(fn: str, code: int) -> None:
+    if code != FP8_OK:
+        raise FP8Error(fn, code)
+
+
+def _stream(stream=None) -> int:
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    return stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+
+
+def _ptr(t: torch.Tensor | None, dtype=None, name="tensor") -> int | None:
+    if t is None:
+        return None
+    if not t.is_cuda:
+        raise ValueError("%s must be a CUDA tensor" % name)
+    if dtype is not None and t.dtype != dtype:
+        raise TypeError("%s must be %s, got %s" % (name, dtype, t.dtype))
+    if not t.is_contiguous():
+        raise ValueError("%s must be contiguous" % name)
+    return t.data_ptr()
+
+
+def _rows(x: torch.Tensor, name: str):
+    if x.dim() != 2:
+        raise ValueError("%s must be 2-D" % name)
+    if x.stride(1) != 1:
+        raise ValueError("%s must have unit column stride" % name)
+    return x.shape[0], x.shape[1], x.stride(0)
+
+
+# ---------------------------------------------------------------- cast
+def fp8_cast_e4m3(x: torch.Tensor, q: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    if q is None:
+        q = torch.empty(x.shape, dtype=torch.uint8, device=x.device)
+    _check("fp8_cast_e4m3", lib.fp8_cast_e4m3(_ptr(x, torch.float32, "x"), x.numel(),
+                                              _ptr(q, torch.uint8, "q"), _stream(stream)))
+    return q
+
+
+# ---------------------------------------------------------------- quantisers
+def fp8_quant_act_1x128(x: torch.Tensor, q=None, s=None, flags: int = 0, stream=None):
+    """x bf16 [M, K] (row stride may exceed K) -> (q u8 [M, K], s f32 [K/128, M])."""
+    M, K, ldx = _rows(x, "x")
+    if x.dtype != torch.bfloat16 or not x.is_cuda:
+        raise TypeError("x must be a CUDA bf16 tensor")
+    q = torch.empty((M, K), dtype=torch.uint8, device=x.device) if q is None else q
+    s = torch.empty((K // 128, M), dtype=torch.float32, device=x.device) if s is None else s
+    _check("fp8_quant_act_1x128", lib.fp8_quant_act_1x128(x.data_ptr(), M, K, ldx, _ptr(q, torch.uint8, "q"),
+                                                          _ptr(s, torch.float32, "s"), flags, _stream(stream)))
+    return q, s
+
+
+def fp8_quant_act_128x1(x: torch.Tensor, qT=None, s=None, flags: int = 0, stream=None):
+    """x bf16 [T, H] -> (qT u8 [H, T], s f32 [T/128, H])."""
+    T, H, ldx = _rows(x, "x")
+    if x.dtype != torch.bfloat16 or not x.is_cuda:
+        raise TypeError("x must be a CUDA bf16 tensor")
+    qT = torch.empty((H, T), dtype=torch.uint8, device=x.device) if qT is None else qT
+    s = torch.empty((T // 128, H), dtype=torch.float32, device=x.device) if s is None else s
+    _check("fp8_quant_act_128x1", lib.fp8_quant_act_128x1(x.data_ptr(), T, H, ldx, _ptr(qT, torch.uint8, "qT"),
+                                                          _ptr(s, torch.float32, "s"), flags, _stream(stream)))
+    return qT, s
+
+
+def fp8_quant_weight_128x128(w: torch.Tensor, q=None, s=None, flags: int = 0, stream=None):
+    """w bf16 [N, K] or [E, N, K] -> (q u8 same shape, s f32 [(E,) N/128, K/128])."""
+    if w.dtype != torch.bfloat16 or not w.is_cuda:
+        raise TypeError("w must be a CUDA bf16 tensor")
+    lead = w.shape[:-2]
+    w2 = w.reshape(-1, w.shape[-1]) if w.dim() == 3 else w
+    N, K, ldw = _rows(w2, "w")
+    q = torch.empty(w.shape, dtype=torch.uint8, device=w.device) if q is None else q
+    s = torch.empty((*lead, w.shape[-2] // 128, K // 128), dtype=torch.float32, device=w.device) if s is None else s
+    _check("fp8_quant_weight_128x128", lib.fp8_quant_weight_128x128(w2.data_ptr(), N, K, ldw,
+                                                                    _ptr(q, torch.uint8, "q"),
+                                                                    _ptr(s, torch.float32, "s"), flags,
+                                                                    _stream(stream)))
+    return q, s
+
+
+# ---------------------------------------------------------------- GEMMs
+def fp8_gemm_blockscaled(a, sa, b, sb, b_scale_mode: int = FP8_BSCALE_BLOCK128, out_dtype=torch.bfloat16,
+                         d=None, stream=None) -> torch.Tensor:
+    """D[M, N] = block-scaled a[M, K] x b[N, K]^T (bf16 or fp32 out)."""
+    M, K = a.shape
+    N = b.shape[0]
+    if b.shape[1] != K:
+        raise ValueError("a and b disagree on K")
+    d_dtype = FP8_OUT_F32 if out_dtype == torch.float32 else FP8_OUT_BF16
+    if d is None:
+        d = torch.empty((M, N), dtype=torch.float32 if d_dtype == FP8_OUT_F32 else torch.bfloat16, device=a.device)
+    _check("fp8_gemm_blockscaled", lib.fp8_gemm_blockscaled(
+        _ptr(a, torch.uint8, "a"), _ptr(sa, torch.float32, "sa"), _ptr(b, torch.uint8, "b"),
+        _ptr(sb, torch.float32, "sb"), b_scale_mode, _ptr(d, None, "d"), d_dtype, M, N, K, _stream(stream)))
+    return d
+
+
+def fp8_grouped_gemm_blockscaled(a, sa, b, sb, expert_offsets, d=None, stream=None) -> torch.Tensor:
+    """Per-expert block-scaled GEMM: a [R, K], b [E, N, K], offsets int32 [E+1] on device -> bf16 [R, N]."""
+    R, K = a.shape
+    E, N, Kb = b.shape
+    if Kb != K:
+        raise ValueError("a and b disagree on K")
+    if d is None:
+        d = torch.empty((R, N), dtype=torch.bfloat16, device=b.device)
+    _check("fp8_grouped_gemm_blockscaled", lib.fp8_grouped_gemm_blockscaled(
+        _ptr(a, torch.uint8, "a"), _ptr(sa, torch.float32, "sa"), _ptr(b, torch.uint8, "b"),
+        _ptr(sb, torch.float32, "sb"), _ptr(expert_offsets, torch.int32, "expert_offsets"), E, R, N, K,
+        _ptr(d, torch.bfloat16, "d"), _stream(stream)))
+    return d
+
+
+# ---------------------------------------------------------------- MoE helpers
+def fp8_moe_route_workspace_size(T: int, E: int) -> int:
+    return lib.fp8_moe_route_workspace_size(T, E)
+
+
+def fp8_moe_route_topk(logits: torch.Tensor, topk: int, out: dict | None = None, work=None, stream=None) -> dict:
+    """logits f32 [T, E] -> dict(idx, gate, off, src_row, pos) on the device."""
+    T, E = logits.shape
+    dev = logits.device
+    o = out or dict(idx=torch.empty((T, topk), dtype=torch.int32, device=dev),
+                    gate=torch.empty((T, topk), dtype=torch.float32, device=dev),
+                    off=torch.empty(E + 1, dtype=torch.int32, device=dev),
+                    src_row=torch.empty(T * topk, dtype=torch.int32, device=dev),
+                    pos=torch.empty((T, topk), dtype=torch.int32, device=dev))
+    if work is None:
+        work = torch.empty(max(1, fp8_moe_route_workspace_size(T, E) // 4), dtype=torch.int32, device=dev)
+    _check("fp8_moe_route_topk", lib.fp8_moe_route_topk(
+        _ptr(logits, torch.float32, "logits"), T, E, topk, _ptr(o["idx"], torch.int32), _ptr(o["gate"], torch.float32),
+        _ptr(o["off"], torch.int32), _ptr(o["src_row"], torch.int32), _ptr(o["pos"], torch.int32),
+        _ptr(work, torch.int32, "work"), _stream(stream)))
+    return o
+
+
+def fp8_permute_rows(q, s, src_row, q_out=None, s_out=None, stream=None):
+    """q u8 [rows, K], s f32 [K/128, rows], src_row int32 [R] -> (q_out [R, K], s_out [K/128, R])."""
+    rows, K = q.shape
+    R = src_row.numel()
+    q_out = torch.empty((R, K), dtype=torch.uint8, device=q.device) if q_out is None else q_out
+    s_out = torch.empty((K // 128, R), dtype=torch.float32, device=q.device) if s_out is None else s_out
+    _check("fp8_permute_rows", lib.fp8_permute_rows(
+        _ptr(q, torch.uint8, "q"), _ptr(s, torch.float32, "s"), rows, K, _ptr(src_row, torch.int32, "src_row"), R,
+        _ptr(q_out, torch.uint8, "q_out"), _ptr(s_out, torch.float32, "s_out"), _stream(stream)))
+    return q_out, s_out
+
+
+def fp8_moe_combine_bf16(y, pos, gate, out=None, stream=None) -> torch.Tensor:
+    """y bf16 [rows, N], pos int32 [T, k], gate f32 [T, k] -> bf16 [T, N]."""
+    rows, N = y.shape
+    T, k = pos.shape
+    out = torch.empty((T, N), dtype=torch.bfloat16, device=y.device) if out is None else out
+    _check("fp8_moe_combine_bf16", lib.fp8_moe_combine_bf16(
+        _ptr(y, torch.bfloat16, "y"), rows, _ptr(pos, torch.int32, "pos"), _ptr(gate, torch.float32, "gate"), T, k, N,
+        _ptr(out, torch.bfloat16, "out"), _stream(stream)))
+    return out
+
+
+def fp8_get_status(stream=None) -> int:
+    """Synchronise the stream; return and clear the device status (0 = ok)."""
+    return lib.fp8_get_status(_stream(stream))
+
+
+def fp8_selftest_wait_timeout(timeout_ns: int, stream=None) -> None:
+    _check("fp8_selftest_wait_timeout", lib.fp8_selftest_wait_timeout(timeout_ns, _stream(stream)))
+
+
+def fp8_strerror(code: int) -> str:
+    return lib.fp8_strerror(code).decode()
+
+
+def fp8_version() -> int:
+    return lib.fp8_version()

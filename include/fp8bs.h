@@ -1,0 +1,242 @@
+/*
+ * fp8bs.h -- C ABI of libfp8bs.so: fine-grained FP8 (E4M3) quantisation and
+ * block-scaled FP8 GEMMs on one B300 GPU (sm_103a).
+ *
+ * The method comes from five scraped web pages that restate DeepSeek-V3's FP8
+ * training recipe.  They are cited as:
+ *   page 1  (why-be.why-be.co.kr, wr_id 35533)  E4M3 on all tensors
+ *   page 2  (tmdrlife.com, wr_id 13334)          limited-width accumulation,
+ *           promotion of partial sums into FP32, power-of-2 scales, the HBM
+ *           round trip of quantised activations
+ *   page 3  (gnrental.net, wr_id 40936)          promotion ("Figure 7 (b)"),
+ *           BF16 combine, microscaling
+ *   page 4  (jp-study.kr, document_srl 258368)   online max-abs per 1x128
+ *           activation tile / 128x128 weight block, quantise before MoE
+ *           dispatch, 256 routed experts with 8 active, 128-element
+ *           accumulation interval, FP8 Wgrad ("Figure 6")
+ *
+ * Conventions for every entry point:
+ *   - Tensor pointers are DEVICE pointers owned by the caller.  The library
+ *     never allocates, frees or keeps them.  bf16 data is passed as raw
+ *     16-bit words (uint16_t), E4M3 data as bytes (uint8_t).
+ *   - Work is enqueued asynchronously on `stream` (a cudaStream_t; NULL is the
+ *     legacy default stream).  No call synchronises the host, except
+ *     fp8_get_status.
+ *   - The return value is FP8_OK (0) or a negative FP8_ERR_* code.  On an
+ *     argument error (FP8_ERR_ARG, _SHAPE, _ALIGN) nothing is enqueued.
+ *     FP8_ERR_CUDA means a launch failed (the CUDA error is left for
+ *     cudaGetLastError to report).
+ *   - Faults found by a kernel while it runs (a pipeline wait that timed out,
+ *     expert offsets out of range) do not trap: the kernel records a code in a
+ *     device status word and exits early.  fp8_get_status reads it.
+ *   - All row-major matrices are dense with the stated leading dimension (in
+ *     elements).  Pointers must be 16-byte aligned and leading dimensions a
+ *     multiple of 16 bytes (FP8_ERR_ALIGN otherwise).
+ *   - E4M3 here is E4M3FN: bias 7, no infinities, largest finite +-448.
+ *     Conversion rounds to nearest-even and saturates to +-448.
+ */
+#ifndef FP8BS_H
+#define FP8BS_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st* fp8_stream_t;   /* same type as cudaStream_t */
+
+#if defined(__GNUC__)
+#define FP8_API __attribute__((visibility("default")))
+#else
+#define FP8_API
+#endif
+
+enum fp8_status {
+    FP8_OK = 0,
+    FP8_ERR_ARG = -1,        /* null pointer, non-positive size, bad enum */
+    FP8_ERR_SHAPE = -2,      /* a dimension that must be a multiple of 128 is not */
+    FP8_ERR_ALIGN = -3,      /* pointer or leading dimension not 16-byte aligned */
+    FP8_ERR_CUDA = -4,       /* a CUDA call or launch failed */
+    FP8_ERR_TIMEOUT = -5,    /* a kernel's bounded pipeline wait expired (device status) */
+    FP8_ERR_OFFSETS = -6,    /* expert offsets not monotone or out of range (device status) */
+    FP8_ERR_DEVICE = -7      /* no usable sm_100-family device */
+};
+
+/* flags of the quantisers */
+#define FP8_SCALE_POW2 1u     /* scales are exact powers of two (pages 2/3) */
+
+/* b_scale_mode of fp8_gemm_blockscaled */
+#define FP8_BSCALE_BLOCK128 0 /* sB [N/128][K/128]: one scale per 128x128 block */
+#define FP8_BSCALE_ROW 1      /* sB [K/128][N]: one scale per B row and K block */
+
+/* d_dtype of fp8_gemm_blockscaled */
+#define FP8_OUT_BF16 0
+#define FP8_OUT_F32 1
+
+/* ------------------------------------------------------------------------
+ * Element-wise E4M3 cast (page 1: E4M3 on all tensors).
+ * q[i] = E4M3(x[i]) with round-to-nearest-even and saturation to +-448; the
+ * same conversion every quantiser uses.  x: n fp32, q: n bytes.  n >= 0.
+ * ---------------------------------------------------------------------- */
+FP8_API int fp8_cast_e4m3(const float* x, int64_t n, uint8_t* q, fp8_stream_t stream);
+
+/* ------------------------------------------------------------------------
+ * 1x128 activation quantiser (page 4: max-abs computed online for each
+ * 1x128 activation tile; page 2: one pass reads the BF16 values and writes
+ * the FP8 codes back to HBM).
+ * For each row m and K block kb, amax = max |x[m][128kb .. 128kb+127]|,
+ * floored at 2^-64.  Default: s = amax/448 and inv = 448/amax (fp32
+ * divisions, rounded to nearest).  FP8_SCALE_POW2: s = 2^e with e the
+ * smallest integer such that 448*2^e >= amax, inv = 2^-e.  Codes are
+ * E4M3(fp32(x * inv)).
+ *   x  bf16 [M][ldx] (K columns used), ldx >= K, ldx % 8 == 0
+ *   q  E4M3 [M][K] row-major
+ *   s  fp32 [K/128][M] (M contiguous: the layout the GEMM reads)
+ * M >= 1, K % 128 == 0.
+ * ---------------------------------------------------------------------- */
+FP8_API int fp8_quant_act_1x128(const uint16_t* x, int64_t M, int64_t K, int64_t ldx,
+                                uint8_t* q, float* s, uint32_t flags, fp8_stream_t stream);
+
+/* ------------------------------------------------------------------------
+ * 128x1 activation quantiser for Wgrad, output transposed (page 4: the
+ * Wgrad operation runs in FP8).  Tiles run along tokens: for each column h
+ * and token block tb, amax over x[128tb .. 128tb+127][h]; scale rule as
+ * above.  The codes are written transposed so that tokens (the K dimension
+ * of Wgrad) are contiguous.
+ *   x   bf16 [T][ldx] (H columns used), ldx >= H, ldx % 8 == 0
+ *   qT  E4M3 [H][T] row-major
+ *   s   fp32 [T/128][H]
+ * T % 128 == 0, H >= 1, H % 8 == 0.
+ * ---------------------------------------------------------------------- */
+FP8_API int fp8_quant_act_128x1(const uint16_t* x, int64_t T, int64_t H, int64_t ldx,
+                                uint8_t* qT, float* s, uint32_t flags, fp8_stream_t stream);
+
+/* ------------------------------------------------------------------------
+ * 128x128 weight quantiser (page 4: max-abs computed online for each
+ * 128x128 weight block).  One scale per block; scale rule as above.
+ *   w  bf16 [N][ldw] (K columns used), ldw >= K, ldw % 8 == 0
+ *   q  E4M3 [N][K]
+ *   s  fp32 [N/128][K/128]
+ * N % 128 == 0, K % 128 == 0.  A stack of E expert matrices [E][N][K] is
+ * quantised in one call as N' = E*N rows (blocks never straddle experts);
+ * its scales are then [E][N/128][K/128].
+ * ---------------------------------------------------------------------- */
+FP8_API int fp8_quant_weight_128x128(const uint16_t* w, int64_t N, int64_t K, int64_t ldw,
+                                     uint8_t* q, float* s, uint32_t flags, fp8_stream_t stream);
+
+/* ------------------------------------------------------------------------
+ * Block-scaled FP8 GEMM (pages 2 and 3: partial sums are accumulated on the
+ * tensor cores over a K interval, then multiplied by the scaling factors and
+ * added into FP32; page 4: the interval is 128 elements).
+ *   D[m][n] = sum_kb  sA[kb][m] * sB(n,kb) * P_kb[m][n],
+ *   P_kb[m][n] = sum_{k in block kb} A[m][k] * B[n][k]   (E4M3 values)
+ * P_kb is formed by tcgen05 MMAs into tensor memory; the outer sum runs in
+ * FP32 registers.
+ *   a   E4M3 [M][K] row-major (K contiguous)
+ *   sa  fp32 [K/128][M]
+ *   b   E4M3 [N][K] row-major (K contiguous)
+ *   sb  b_scale_mode FP8_BSCALE_BLOCK128: fp32 [N/128][K/128]
+ *       b_scale_mode FP8_BSCALE_ROW:      fp32 [K/128][N]
+ *   d   [M][N] row-major, bf16 (FP8_OUT_BF16, rounded to nearest-even) or
+ *       fp32 (FP8_OUT_F32)
+ * M >= 1, N % 128 == 0, K % 128 == 0.  Wgrad (dW = dY^T X) is this call with
+ * a = dY^T and b = X^T from fp8_quant_act_128x1, FP8_BSCALE_ROW, FP8_OUT_F32.
+ * ---------------------------------------------------------------------- */
+FP8_API int fp8_gemm_blockscaled(const uint8_t* a, const float* sa,
+                                 const uint8_t* b, const float* sb, int b_scale_mode,
+                                 void* d, int d_dtype, int64_t M, int64_t N, int64_t K,
+                                 fp8_stream_t stream);
+
+/* ------------------------------------------------------------------------
+ * Grouped (per-expert) block-scaled FP8 GEMM for MoE (page 4: 256 routed
+ * experts; each expert processes the rows dispatched to it).  Expert e owns
+ * rows [off[e], off[e+1]) of a and d and multiplies them by its own B_e:
+ *   d[r][n] = sum_kb sa[kb][r] * sb[e][n/128][kb] * P_kb(a[r], b[e][n])
+ *   a    E4M3 [total_rows][K] (rows grouped by expert)
+ *   sa   fp32 [K/128][total_rows]
+ *   b    E4M3 [E][N][K]
+ *   sb   fp32 [E][N/128][K/128]
+ *   off  int32 [E+1] on the DEVICE: off[0] = 0, non-decreasing,
+ *        off[E] = total_rows.  Empty experts are allowed.  The host never
+ *        reads it.  Offsets that break these rules make the kernel record
+ *        FP8_ERR_OFFSETS in the device status and skip the bad experts.
+ *   d    bf16 [total_rows][N]
+ * 1 <= E <= 1024, total_rows >= 0, N % 128 == 0, K % 128 == 0.
+ * ---------------------------------------------------------------------- */
+FP8_API int fp8_grouped_gemm_blockscaled(const uint8_t* a, const float* sa,
+                                         const uint8_t* b, const float* sb,
+                                         const int32_t* expert_offsets, int E,
+                                         int64_t total_rows, int64_t N, int64_t K,
+                                         uint16_t* d, fp8_stream_t stream);
+
+/* ------------------------------------------------------------------------
+ * MoE routing on one GPU (page 4: each token activates 8 of 256 routed
+ * experts).  Top-k of each token's logits, ties going to the lower expert
+ * index; gates = softmax over the k selected logits (fp32); dispatch order =
+ * (token, slot) pairs stably sorted by expert.
+ *   logits  fp32 [T][E]
+ *   idx     int32 [T][topk]   selected experts, highest logit first
+ *   gate    fp32  [T][topk]
+ *   off     int32 [E+1]       exclusive prefix sum of rows per expert
+ *   src_row int32 [T*topk]    dispatched row p holds token src_row[p]
+ *   pos     int32 [T][topk]   row that (token, slot) was dispatched to
+ *   work    int32 scratch of fp8_moe_route_workspace_size(T, E) bytes; its
+ *           contents on entry do not matter
+ * 1 <= E <= 1024, 1 <= topk <= min(E, 32), T >= 1.
+ * ---------------------------------------------------------------------- */
+FP8_API int64_t fp8_moe_route_workspace_size(int64_t T, int E);
+FP8_API int fp8_moe_route_topk(const float* logits, int64_t T, int E, int topk,
+                               int32_t* idx, float* gate, int32_t* expert_offsets,
+                               int32_t* src_row, int32_t* pos, int32_t* work,
+                               fp8_stream_t stream);
+
+/* ------------------------------------------------------------------------
+ * Dispatch on one GPU: gather FP8 rows and their scales (page 4: activations
+ * are quantised before the MoE up-projection, then dispatched in FP8).
+ *   q_out[p][:] = q[src_row[p]][:],  s_out[kb][p] = s[kb][src_row[p]]
+ *   q [rows][K], s [K/128][rows], src_row int32 [out_rows] (values in
+ *   [0, rows)), q_out [out_rows][K], s_out [K/128][out_rows].  K % 128 == 0.
+ * An index out of range records FP8_ERR_OFFSETS and that row is zero-filled.
+ * ---------------------------------------------------------------------- */
+FP8_API int fp8_permute_rows(const uint8_t* q, const float* s, int64_t rows, int64_t K,
+                             const int32_t* src_row, int64_t out_rows,
+                             uint8_t* q_out, float* s_out, fp8_stream_t stream);
+
+/* ------------------------------------------------------------------------
+ * Combine kept in BF16 (page 3: forward and backward combine stay in BF16):
+ *   out[t][n] = bf16( sum_{j < topk} gate[t][j] * y[pos[t][j]][n] )
+ * summed in fp32 in slot order, rounded to nearest-even once.
+ *   y bf16 [rows][N], pos int32 [T][topk] (values in [0, rows)),
+ *   gate fp32 [T][topk], out bf16 [T][N].  N % 8 == 0.
+ * An index out of range records FP8_ERR_OFFSETS and contributes zero.
+ * ---------------------------------------------------------------------- */
+FP8_API int fp8_moe_combine_bf16(const uint16_t* y, int64_t rows, const int32_t* pos,
+                                 const float* gate, int64_t T, int topk, int64_t N,
+                                 uint16_t* out, fp8_stream_t stream);
+
+/* ------------------------------------------------------------------------
+ * Device status: synchronises `stream`, then returns and clears the first
+ * error code that a kernel recorded on the current device (FP8_OK if none).
+ * ---------------------------------------------------------------------- */
+FP8_API int fp8_get_status(fp8_stream_t stream);
+
+/* ------------------------------------------------------------------------
+ * Failure-detection self-test (no counterpart on the pages): launches one
+ * thread that waits on a pipeline barrier nobody arrives on, with the same
+ * bounded wait the GEMMs use, shortened to timeout_ns (1 ns .. 2 s).  The
+ * wait gives up, FP8_ERR_TIMEOUT is recorded in the device status, and the
+ * kernel exits normally; fp8_get_status then returns FP8_ERR_TIMEOUT.
+ * ---------------------------------------------------------------------- */
+FP8_API int fp8_selftest_wait_timeout(uint64_t timeout_ns, fp8_stream_t stream);
+
+/* Human-readable name of a status code (static string). */
+FP8_API const char* fp8_strerror(int code);
+
+/* Library ABI version (major*100 + minor). */
+FP8_API int fp8_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* FP8BS_H */

@@ -1,0 +1,104 @@
+"""The C-ABI library loads without a GPU, exports every entry point the
+header declares, and rejects bad arguments before touching the device."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "fp8bs.h")
+
+
+@pytest.fixture(scope="module")
+def fb():
+    from fp8_fine_grained_16_b300 import build
+    build.build()
+    from fp8_fine_grained_16_b300 import fp8bs
+    return fp8bs
+
+
+def declared_symbols():
+    text = open(HEADER).read()
+    return sorted(set(re.findall(r"^FP8_API\s+[\w\s\*]+?\b(fp8_\w+)\s*\(", text, flags=re.M)))
+
+
+def test_header_declares_the_five_hot_path_calls():
+    syms = declared_symbols()
+    for name in ["fp8_quant_act_1x128", "fp8_quant_act_128x1", "fp8_quant_weight_128x128",
+                 "fp8_gemm_blockscaled", "fp8_grouped_gemm_blockscaled"]:
+        assert name in syms
+
+
+def test_library_exports_every_declared_symbol(fb):
+    syms = declared_symbols()
+    assert syms == fb.EXPORTED
+    lib = ctypes.CDLL(fb.LIB_PATH)
+    for s in syms:
+        assert hasattr(lib, s), s
+
+
+def test_version_and_strerror(fb):
+    assert fb.fp8_version() == 100
+    assert fb.fp8_strerror(0) == "ok"
+    assert "timed out" in fb.fp8_strerror(-5)
+    assert fb.fp8_strerror(12345) == "unknown status"
+
+
+def test_workspace_size(fb):
+    assert fb.fp8_moe_route_workspace_size(4096, 256) == 64 * 256 * 4
+    assert fb.fp8_moe_route_workspace_size(65, 8) == 2 * 8 * 4
+    assert fb.fp8_moe_route_workspace_size(0, 8) == 0
+
+
+# Argument checks run on the host before any CUDA call, so they are testable
+# here; a fake but aligned device address stands in for real buffers.
+FAKE = 1 << 40
+
+
+def test_quant_argument_errors(fb):
+    L = fb.lib
+    assert L.fp8_quant_act_1x128(None, 4, 128, 128, FAKE, FAKE, 0, None) == -1          # null x
+    assert L.fp8_quant_act_1x128(FAKE, 0, 128, 128, FAKE, FAKE, 0, None) == -1          # M = 0
+    assert L.fp8_quant_act_1x128(FAKE, 4, 100, 100, FAKE, FAKE, 0, None) == -2          # K % 128
+    assert L.fp8_quant_act_1x128(FAKE + 2, 4, 128, 128, FAKE, FAKE, 0, None) == -3      # misaligned x
+    assert L.fp8_quant_act_1x128(FAKE, 4, 128, 130, FAKE, FAKE, 0, None) == -3          # ldx % 8
+    assert L.fp8_quant_act_1x128(FAKE, 4, 128, 128, FAKE, FAKE, 6, None) == -1          # unknown flag
+    assert L.fp8_quant_act_128x1(FAKE, 100, 64, 64, FAKE, FAKE, 0, None) == -2          # T % 128
+    assert L.fp8_quant_act_128x1(FAKE, 128, 12, 12, FAKE, FAKE, 0, None) == -2          # H % 8
+    assert L.fp8_quant_weight_128x128(FAKE, 100, 128, 128, FAKE, FAKE, 0, None) == -2   # N % 128
+    assert L.fp8_cast_e4m3(None, 5, FAKE, None) == -1
+    assert L.fp8_cast_e4m3(None, 0, None, None) == 0                                    # empty: no-op
+
+
+def test_gemm_argument_errors(fb):
+    L = fb.lib
+    base = dict(a=FAKE, sa=FAKE, b=FAKE, sb=FAKE, mode=0, d=FAKE, dt=0, M=128, N=256, K=256, st=None)
+
+    def call(**kw):
+        a = dict(base, **kw)
+        return L.fp8_gemm_blockscaled(*a.values())
+
+    assert call(a=None) == -1
+    assert call(mode=2) == -1
+    assert call(dt=7) == -1
+    assert call(K=200) == -2
+    assert call(N=200) == -2
+    assert call(d=FAKE + 4) == -3
+    assert call(M=0) == -1
+    g = fb.lib.fp8_grouped_gemm_blockscaled
+    assert g(FAKE, FAKE, FAKE, FAKE, FAKE, 0, 10, 256, 256, FAKE, None) == -1            # E = 0
+    assert g(FAKE, FAKE, FAKE, FAKE, FAKE, 2000, 10, 256, 256, FAKE, None) == -1         # E too large
+    assert g(FAKE, FAKE, FAKE, FAKE, FAKE, 4, 10, 256, 200, FAKE, None) == -2            # K % 128
+    assert g(None, None, FAKE, FAKE, FAKE, 4, 0, 256, 256, None, None) == 0              # no rows: no-op
+
+
+def test_moe_argument_errors(fb):
+    L = fb.lib
+    assert L.fp8_moe_route_topk(FAKE, 16, 8, 9, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, None) == -1   # topk > E
+    assert L.fp8_moe_route_topk(FAKE, 16, 2048, 8, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, None) == -1
+    assert L.fp8_moe_route_topk(FAKE + 2, 16, 8, 2, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, None) == -3
+    assert L.fp8_permute_rows(FAKE, FAKE, 10, 100, FAKE, 5, FAKE, FAKE, None) == -2
+    assert L.fp8_permute_rows(None, None, 10, 128, None, 0, None, None, None) == 0
+    assert L.fp8_moe_combine_bf16(FAKE, 10, FAKE, FAKE, 4, 2, 12, FAKE, None) == -2
+    assert L.fp8_selftest_wait_timeout(0, None) == -1
