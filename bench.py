@@ -1,0 +1,464 @@
+"""Benchmark of the fine-grained FP8 path on B300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference] [--rows all|none]
+
+One step = one pass of the dense-linear workload through the whole path:
+1x128 quantisation of X [4096, 7168], 128x128 quantisation of W [7168, 7168]
+and the block-scaled FP8 GEMM -> bf16 Y [4096, 7168], inputs resident in
+HBM.  The headline value is the step's GEMM FLOPs / step time (TFLOP/s).
+Between timed steps L2 is flushed by writing a 256 MiB buffer (outside each
+step's events).  Rank 0 prints one JSON line.
+
+Besides the headline, ``rows`` times every step of the path on its own
+workload (the 128x1 quantiser and Wgrad GEMM, the grouped MoE GEMMs, routing,
+dispatch and combine) against its roofline.
+
+With N > 1 (torchrun) every rank runs the same workload independently: the
+path has no exchange step on one GPU, so this is N replicas (weak scaling);
+the step time is the max over ranks.
+
+``--impl reference`` times the CPU oracle (the plain definition of what the
+path computes) on a bounded sample of the same workload, on rank 0 only.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+M, N, K = 4096, 7168, 7168
+GEMM_FLOP = 2.0 * M * N * K
+FP8_NOMINAL_TFLOPS = 4500.0           # dense E4M3, nominal
+HBM_NOMINAL_GBS = 8000.0
+METRIC = "FP8 block-scaled GEMM TFLOP/s (% FP8 peak); quantize GB/s (% HBM peak)"
+WORKLOAD = ("dense linear: X bf16 [4096,7168] ~0.5*t(3), W bf16 [7168,7168] ~N(0,0.02^2); "
+            "quantise X 1x128 + quantise W 128x128 + block-scaled FP8 GEMM -> bf16 [4096,7168]")
+
+
+# ---------------------------------------------------------------- helpers
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return dict(hbm=float(d["hbm_gbs"]), bf16=float(d["bf16_tflops"]),
+                    bf16_sustained=float(d.get("bf16_tflops_sustained", d["bf16_tflops"])), src="measured")
+    return dict(hbm=6400.0, bf16=1800.0, bf16_sustained=1400.0, src="fallback")
+
+
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+class Clocks:
+    """nvidia-smi sampled every 100 ms while the timed region runs."""
+
+    def __init__(self, index: int):
+        self.index = index
+        fd, self.path = tempfile.mkstemp(prefix="clocks", suffix=".csv")
+        os.close(fd)
+        self.proc = None
+
+    def __enter__(self):
+        q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+        try:
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.index), "--query-gpu=" + q,
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                         stdout=self.f, stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+        return self
+
+    def __exit__(self, *a):
+        if self.proc:
+            self.proc.terminate()
+            self.proc.wait()
+            self.f.close()
+
+    def summary(self):
+        if not self.proc:
+            return None
+        rows = []
+        for line in open(self.path):
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                rows.append(dict(sm=float(f[1]), smax=float(f[2]), power=float(f[3]),
+                                 hw=f[5] == "Active", hwt=f[6] == "Active", swt=f[7] == "Active",
+                                 cap=f[8] == "Active"))
+            except ValueError:
+                pass
+        os.unlink(self.path)
+        if not rows:
+            return None
+        reasons = []
+        for key, name in (("hw", "hw_slowdown"), ("hwt", "hw_thermal_slowdown"),
+                          ("swt", "sw_thermal_slowdown"), ("cap", "sw_power_cap")):
+            if any(r[key] for r in rows):
+                reasons.append(name)
+        return dict(sm_mhz=statistics.median(r["sm"] for r in rows), sm_max_mhz=max(r["smax"] for r in rows),
+                    reasons=reasons, samples=len(rows), power_w_max=max(r["power"] for r in rows))
+
+
+def kernel_source_sha():
+    h = hashlib.sha256()
+    for f in ("gemm.cu", "common.cuh"):
+        h.update(open(os.path.join(ROOT, "fp8_fine_grained_16_b300", "csrc", f), "rb").read())
+    return h.hexdigest()[:16]
+
+
+def ncu_traffic():
+    """DRAM bytes per launch of the dense-linear GEMM from the committed ncu
+    summary, if it was taken on the current kernel source."""
+    p = os.path.join(ROOT, "profiles", "gemm_dense_linear_traffic.json")
+    if not os.path.exists(p):
+        return None
+    d = json.load(open(p))
+    if d.get("kernel_src_sha") != kernel_source_sha():
+        return None
+    return d.get("dram_bytes_per_launch")
+
+
+# ---------------------------------------------------------------- our arm
+def run_ours(args, ws, rank, local):
+    from fp8_fine_grained_16_b300 import build
+    build.build()
+    from fp8_fine_grained_16_b300 import fp8bs as F
+    from fp8_fine_grained_16_b300 import synthetic as S
+
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    stream = torch.cuda.current_stream()
+    pk = peaks()
+
+    d = S.dense_linear()
+    x_h, w_h = d["x"].pin_memory(), d["w"].pin_memory()
+    x, w = x_h.to(dev), w_h.to(dev)
+    qx = torch.empty((M, K), dtype=torch.uint8, device=dev)
+    sx = torch.empty((K // 128, M), dtype=torch.float32, device=dev)
+    qw = torch.empty((N, K), dtype=torch.uint8, device=dev)
+    sw = torch.empty((N // 128, K // 128), dtype=torch.float32, device=dev)
+    y = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+
+    def step(evs=None):
+        if evs:
+            evs[0].record(stream)
+        F.fp8_quant_act_1x128(x, qx, sx)
+        if evs:
+            evs[1].record(stream)
+        F.fp8_quant_weight_128x128(w, qw, sw)
+        if evs:
+            evs[2].record(stream)
+        F.fp8_gemm_blockscaled(qx, sx, qw, sw, 0, torch.bfloat16, d=y)
+        if evs:
+            evs[3].record(stream)
+
+    for _ in range(args.warmup):
+        flush.zero_()
+        step()
+    torch.cuda.synchronize()
+    if F.fp8_get_status() != 0:
+        raise RuntimeError("device status set during warm-up")
+
+    # Timed region: the GPU runs flush, step, flush, step, ... back to back
+    # (no host synchronisation inside), each step bracketed by its own events.
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
+    if ws > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    with Clocks(local) as clk:
+        for i in range(args.steps):
+            flush.zero_()
+            step(evs[i])
+        torch.cuda.synchronize()
+    if ws > 1:
+        torch.distributed.barrier()
+    t_step = [e[0].elapsed_time(e[3]) for e in evs]
+    t_qx = [e[0].elapsed_time(e[1]) for e in evs]
+    t_qw = [e[1].elapsed_time(e[2]) for e in evs]
+    t_gemm = [e[2].elapsed_time(e[3]) for e in evs]
+    if F.fp8_get_status() != 0:
+        raise RuntimeError("device status set during the timed steps")
+    ms = sum(t_step) / len(t_step)
+    if ws > 1:
+        t = torch.tensor([ms], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        ms = float(t.item())
+    clocks = clk.summary()
+
+    gemm_ms = sum(t_gemm) / len(t_gemm)
+    qx_ms = sum(t_qx) / len(t_qx)
+    qw_ms = sum(t_qw) / len(t_qw)
+    fp8_peak = pk["bf16"] * 2.0             # E4M3 dense = 2x bf16 dense (nominal 4.5 / 2.25 PFLOP/s)
+    achieved = GEMM_FLOP / (gemm_ms * 1e-3) / 1e12
+
+    # ---- end to end through the public API from pinned host buffers
+    y_h = torch.empty((M, N), dtype=torch.bfloat16).pin_memory()
+    e_start, e_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e2e_ms = []
+    e2e_steps = min(args.steps, 30)
+    for i in range(args.warmup + e2e_steps):
+        flush.zero_()
+        torch.cuda.synchronize()
+        e_start.record(stream)
+        x.copy_(x_h, non_blocking=True)
+        w.copy_(w_h, non_blocking=True)
+        step()
+        y_h.copy_(y, non_blocking=True)
+        e_end.record(stream)
+        e_end.synchronize()
+        if i >= args.warmup:
+            e2e_ms.append(e_start.elapsed_time(e_end))
+    e2e = sum(e2e_ms) / len(e2e_ms)
+
+    rows = measure_rows(F, S, dev, flush, pk) if args.rows == "all" else None
+
+    out = {
+        "metric": METRIC,
+        "value": round(GEMM_FLOP * ws / (ms * 1e-3) / 1e12, 2),
+        "unit": "TFLOP/s",
+        "n_gpus": ws,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(ms, 5),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "e4m3 (fp32 accumulate, bf16 out)",
+        "data": "synthetic",
+        "config": {"workload": WORKLOAD, "l2": "flushed between steps (256 MiB write)",
+                   "parallelism": "replicas" if ws > 1 else "single GPU"},
+        "roofline": {"bound": "tensor", "kernel": "gemm_blockscaled (dense linear 4096x7168x7168)",
+                     "achieved": round(achieved, 1), "peak": round(fp8_peak, 1), "unit": "TFLOP/s",
+                     "frac": round(achieved / fp8_peak, 4),
+                     "peak_source": "%s bf16 burst x 2 (E4M3/bf16 nominal ratio)" % pk["src"],
+                     "frac_of_nominal_4500": round(achieved / FP8_NOMINAL_TFLOPS, 4),
+                     "traffic": ncu_traffic()},
+        "step_breakdown_ms": {"quant_act_1x128": round(qx_ms, 5), "quant_weight_128x128": round(qw_ms, 5),
+                              "gemm": round(gemm_ms, 5)},
+        "e2e": {"value": round(GEMM_FLOP * ws / (e2e * 1e-3) / 1e12, 3), "unit": "TFLOP/s",
+                "ms_per_step": round(e2e, 4), "steps": e2e_steps,
+                "h2d_bytes_per_step": x.numel() * 2 + w.numel() * 2, "d2h_bytes_per_step": y.numel() * 2},
+        "gpu_launches": 3 * args.steps,     # quant_act_1x128, quant_weight_128x128, gemm per step
+        "clocks": clocks,
+    }
+    if rows is not None:
+        out["rows"] = rows
+    if rank == 0 and ws == 1 and not args.no_cpu_baseline:
+        out["cpu_baseline"] = cpu_baseline(S, d=d)
+    return out
+
+
+def _time(fn, reps, warm, flush, stream):
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    for _ in range(warm):
+        fn()
+    ts = []
+    for _ in range(reps):
+        flush.zero_()
+        a.record(stream)
+        fn()
+        b.record(stream)
+        b.synchronize()
+        ts.append(a.elapsed_time(b))
+    return statistics.median(ts)
+
+
+def measure_rows(F, S, dev, flush, pk):
+    """Each step of the path on its own workload, median of timed reps."""
+    st = torch.cuda.current_stream()
+    reps, warm = 20, 3
+    fp8_peak = pk["bf16"] * 2.0
+    out = {}
+
+    def hbm_row(name, ms, nbytes, workload):
+        gbs = nbytes / (ms * 1e-3) / 1e9
+        out[name] = dict(workload=workload, ms=round(ms, 5), bound="hbm", achieved=round(gbs, 1), unit="GB/s",
+                         algorithmic_bytes=int(nbytes), peak=pk["hbm"], frac=round(gbs / pk["hbm"], 4),
+                         frac_of_nominal_8000=round(gbs / HBM_NOMINAL_GBS, 4))
+
+    def tensor_row(name, ms, flop, workload, extra=None):
+        tf = flop / (ms * 1e-3) / 1e12
+        r = dict(workload=workload, ms=round(ms, 5), bound="tensor", achieved=round(tf, 1), unit="TFLOP/s",
+                 flop=flop, peak=round(fp8_peak, 1), frac=round(tf / fp8_peak, 4),
+                 frac_of_nominal_4500=round(tf / FP8_NOMINAL_TFLOPS, 4))
+        if extra:
+            r.update(extra)
+        out[name] = r
+
+    # dense linear rows
+    d = S.dense_linear()
+    x, w = d["x"].to(dev), d["w"].to(dev)
+    qx, sx = F.fp8_quant_act_1x128(x)
+    qw, sw = F.fp8_quant_weight_128x128(w)
+    y = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+    ms = _time(lambda: F.fp8_quant_act_1x128(x, qx, sx), reps, warm, flush, st)
+    hbm_row("a1_quant_act_1x128", ms, M * K * 3 + M * (K // 128) * 4, "X [4096,7168]")
+    ms = _time(lambda: F.fp8_quant_weight_128x128(w, qw, sw), reps, warm, flush, st)
+    hbm_row("a3_quant_weight_128x128", ms, N * K * 3 + (N // 128) * (K // 128) * 4, "W [7168,7168]")
+    ms = _time(lambda: F.fp8_gemm_blockscaled(qx, sx, qw, sw, 0, torch.bfloat16, d=y), reps, warm, flush, st)
+    tensor_row("a4_gemm_dense", ms, GEMM_FLOP, "4096x7168x7168 -> bf16")
+    del x, w, qx, qw, y
+
+    # Wgrad rows
+    d = S.wgrad()
+    T, H = d["dy"].shape
+    dy, xx = d["dy"].to(dev), d["x"].to(dev)
+    qa, sa = F.fp8_quant_act_128x1(dy)
+    qb, sb = F.fp8_quant_act_128x1(xx)
+    dw = torch.empty((H, H), dtype=torch.float32, device=dev)
+    ms = _time(lambda: F.fp8_quant_act_128x1(dy, qa, sa), reps, warm, flush, st)
+    hbm_row("a2_quant_act_128x1", ms, T * H * 3 + (T // 128) * H * 4, "dY [8192,7168] -> dY^T")
+    ms = _time(lambda: F.fp8_gemm_blockscaled(qa, sa, qb, sb, F.FP8_BSCALE_ROW, torch.float32, d=dw),
+               reps, warm, flush, st)
+    tensor_row("a5_gemm_wgrad", ms, 2.0 * H * H * T, "dW = dY^T X, 7168x7168x8192 -> fp32")
+    del dy, xx, qa, qb, dw
+
+    # MoE up-proj
+    E, k = 256, 8
+    mu = S.moe_up(with_weights=False)
+    x, logits = mu["x"].to(dev), mu["logits"].to(dev)
+    Tn = x.shape[0]
+    r = F.fp8_moe_route_topk(logits, k)
+    ms = _time(lambda: F.fp8_moe_route_topk(logits, k, out=r), reps, warm, flush, st)
+    out["a7_route_topk"] = dict(workload="logits [4096,256] -> top-8", ms=round(ms, 5), bound="latency")
+    qx, sx = F.fp8_quant_act_1x128(x)
+    qa, sa = F.fp8_permute_rows(qx, sx, r["src_row"])
+    ms = _time(lambda: F.fp8_permute_rows(qx, sx, r["src_row"], qa, sa), reps, warm, flush, st)
+    R = Tn * k
+    hbm_row("a7_permute_rows", ms, 2 * R * (K + (K // 128) * 4) + R * 4, "[4096,7168] fp8 -> [32768,7168]")
+    Nu = 4096
+    wst = S.expert_weights(0, E, Nu, K, device=dev)
+    qwu, swu = F.fp8_quant_weight_128x128(wst)
+    ms = _time(lambda: F.fp8_quant_weight_128x128(wst, qwu, swu), 3, 1, flush, st)
+    hbm_row("a3_quant_weight_moe_up", ms, E * Nu * K * 3 + E * (Nu // 128) * (K // 128) * 4, "256 x [4096,7168]")
+    del wst
+    yu = torch.empty((R, Nu), dtype=torch.bfloat16, device=dev)
+    ms = _time(lambda: F.fp8_grouped_gemm_blockscaled(qa, sa, qwu, swu, r["off"], d=yu), reps, warm, flush, st)
+    wbytes = E * Nu * K
+    moved = wbytes + R * K + R * Nu * 2
+    tensor_row("a6_grouped_moe_up", ms, 2.0 * R * Nu * K, "32768 rows, 256 experts, N=4096, K=7168",
+               dict(weight_bytes=wbytes, hbm_achieved_gbs=round(moved / (ms * 1e-3) / 1e9, 1),
+                    hbm_frac=round(moved / (ms * 1e-3) / 1e9 / pk["hbm"], 4)))
+    del qwu, yu, qa, qx
+
+    # MoE down-proj + combine
+    md = S.moe_down(with_weights=False)
+    h, logits = md["h"].to(dev), md["logits"].to(dev)
+    r = F.fp8_moe_route_topk(logits, k)
+    Kd, Nd = 2048, 7168
+    qh, sh = F.fp8_quant_act_1x128(h)
+    ms = _time(lambda: F.fp8_quant_act_1x128(h, qh, sh), reps, warm, flush, st)
+    hbm_row("a1_quant_act_1x128_moe_down", ms, R * Kd * 3 + R * (Kd // 128) * 4, "h [32768,2048]")
+    wst = S.expert_weights(1, E, Nd, Kd, device=dev)
+    qwd, swd = F.fp8_quant_weight_128x128(wst)
+    del wst
+    yd = torch.empty((R, Nd), dtype=torch.bfloat16, device=dev)
+    ms = _time(lambda: F.fp8_grouped_gemm_blockscaled(qh, sh, qwd, swd, r["off"], d=yd), reps, warm, flush, st)
+    wbytes = E * Nd * Kd
+    moved = wbytes + R * Kd + R * Nd * 2
+    tensor_row("a6_grouped_moe_down", ms, 2.0 * R * Nd * Kd, "32768 rows, 256 experts, N=7168, K=2048",
+               dict(weight_bytes=wbytes, hbm_achieved_gbs=round(moved / (ms * 1e-3) / 1e9, 1),
+                    hbm_frac=round(moved / (ms * 1e-3) / 1e9 / pk["hbm"], 4)))
+    outc = torch.empty((Tn, Nd), dtype=torch.bfloat16, device=dev)
+    ms = _time(lambda: F.fp8_moe_combine_bf16(yd, r["pos"], r["gate"], out=outc), reps, warm, flush, st)
+    hbm_row("a7_combine_bf16", ms, R * Nd * 2 + Tn * Nd * 2 + R * 8, "[32768,7168] bf16 -> [4096,7168]")
+    torch.cuda.synchronize()
+    if F.fp8_get_status() != 0:
+        raise RuntimeError("device status set while timing rows")
+    return out
+
+
+# ---------------------------------------------------------------- oracle (CPU) arm
+def cpu_baseline(S, rows=384, d=None):
+    """The oracle, as it stands, on a bounded sample of the dense-linear step:
+    1x128 quantisation of `rows` rows of X, 128x128 quantisation of all of W,
+    and those rows of the GEMM.  Reported as GEMM TFLOP/s of the sample."""
+    import oracle
+    oracle.build()
+    d = d or S.dense_linear()
+    xb = S.bf16_bits(d["x"][:rows])
+    wb = S.bf16_bits(d["w"])
+    t0 = time.perf_counter()
+    qa, sa = oracle.quant_act_1x128(xb)
+    qb, sb = oracle.quant_weight_128x128(wb)
+    oracle.gemm_blockscaled(qa, sa, qb, sb, 0)
+    dt = time.perf_counter() - t0
+    flop = 2.0 * rows * N * K
+    return {"value": round(flop / dt / 1e12, 6), "unit": "TFLOP/s", "cores": oracle.max_threads(),
+            "kind": "oracle", "seconds": round(dt, 2),
+            "sample": "%d of 4096 rows of the dense-linear step (quantise those X rows, all of W, and their "
+                      "GEMM rows in fp64)" % rows}
+
+
+def run_reference(args, ws, rank):
+    from fp8_fine_grained_16_b300 import synthetic as S
+    if rank != 0:
+        return None
+    per = []
+    cb = None
+    d = S.dense_linear()
+    for i in range(args.warmup + args.steps):
+        cb = cpu_baseline(S, rows=8, d=d)
+        if i >= args.warmup:
+            per.append(cb["seconds"])
+    flop = 2.0 * 8 * N * K
+    ms = 1e3 * sum(per) / len(per)
+    v = round(flop / (ms * 1e-3) / 1e12, 6)
+    cb["value"] = v
+    return {
+        "impl": "reference", "metric": METRIC, "value": v, "unit": "TFLOP/s", "n_gpus": ws,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 3), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64 (oracle)", "data": "synthetic",
+        "config": {"workload": WORKLOAD + " -- oracle on 8 rows per step", "l2": "n/a (CPU)"},
+        "cpu_baseline": cb,
+        "e2e": {"value": v, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=1000)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--rows", choices=["all", "none"], default="all")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    ws, rank, local = dist_env()
+    if args.impl == "reference":
+        out = run_reference(args, ws, rank)
+        if out is not None:
+            print(json.dumps(out))
+        return
+    if ws > 1:
+        torch.distributed.init_process_group("nccl", device_id=torch.device("cuda", local))
+    out = run_ours(args, ws, rank, local)
+    if rank == 0:
+        print(json.dumps(out))
+    if ws > 1:
+        torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()
