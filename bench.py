@@ -388,7 +388,7 @@ def measure_rows(F, S, dev, flush, pk):
 
 
 # ---------------------------------------------------------------- oracle (CPU) arm
-def cpu_baseline(S, rows=384, d=None):
+def cpu_baseline(S, rows=4096, d=None):
     """The oracle, as it stands, on a bounded sample of the dense-linear step:
     1x128 quantisation of `rows` rows of X, 128x128 quantisation of all of W,
     and those rows of the GEMM.  Reported as GEMM TFLOP/s of the sample."""
