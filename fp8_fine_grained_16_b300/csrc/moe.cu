@@ -11,6 +11,8 @@
 //                         same expert (64-bit token masks + popcount)
 //   permute   gathers FP8 rows and their K-block scales (dispatch)
 //   combine   out[t] = sum_j gate[t][j] * y[pos[t][j]] in fp32 -> bf16
+#include <mutex>
+
 #include "common.cuh"
 
 namespace fp8bs {
@@ -315,6 +317,48 @@ extern "C" int fp8_moe_combine_bf16(const uint16_t* y, int64_t rows, const int32
     moe_combine_kernel<<<unsigned(blocks < cap ? blocks : cap), 256, 0, reinterpret_cast<cudaStream_t>(stream)>>>(
         y, rows, pos, gate, T, topk, N, out);
     return cudaGetLastError() == cudaSuccess ? FP8_OK : FP8_ERR_CUDA;
+}
+
+// ------------------------------------------------------------------ routing without caller scratch
+// Variant of fp8_moe_route_topk for callers that cannot allocate device
+// memory where they call it.  The per-chunk expert counts live in this
+// file-scope device array instead of a caller buffer; every GPU that loads
+// the library keeps it (1 MiB) until the process exits.  No element needs to
+// start at zero: the first kernel writes all nchunks x E counts before the
+// second kernel reads any of them, in the same call.  Calls share the array,
+// so two calls whose kernels overlap on the GPU race on it.
+namespace fp8bs {
+static __device__ __align__(256) int32_t g_route_scratch[FP8_ROUTE_NOALLOC_MAX_WORK];
+
+constexpr int kMaxDevices = 64;
+
+// Device address of g_route_scratch for the current device.  In host code
+// the array's name is only a host-side stand-in, so the address comes from
+// cudaGetSymbolAddress, once per device, with that device current.
+static int32_t* route_scratch_address() {
+    static std::mutex mu;
+    static int32_t* addr[kMaxDevices] = {};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+    std::lock_guard<std::mutex> lock(mu);
+    if (!addr[dev]) {
+        void* p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_route_scratch) != cudaSuccess || !p) return nullptr;
+        addr[dev] = static_cast<int32_t*>(p);
+    }
+    return addr[dev];
+}
+}  // namespace fp8bs
+
+extern "C" int fp8_moe_route_topk_noalloc(const float* logits, int64_t T, int E, int topk, int32_t* idx, float* gate,
+                                          int32_t* expert_offsets, int32_t* src_row, int32_t* pos,
+                                          fp8_stream_t stream) {
+    if (T <= 0 || E <= 0 || E > kMaxE || topk <= 0 || topk > kMaxK || topk > E) return FP8_ERR_ARG;
+    if (fp8_moe_route_workspace_size(T, E) > int64_t(sizeof(int32_t)) * FP8_ROUTE_NOALLOC_MAX_WORK)
+        return FP8_ERR_SCRATCH;
+    int32_t* work = route_scratch_address();
+    if (!work) return FP8_ERR_CUDA;
+    return fp8_moe_route_topk(logits, T, E, topk, idx, gate, expert_offsets, src_row, pos, work, stream);
 }
 
 extern "C" int fp8bs_moe_take_status(cudaStream_t stream) {

@@ -21,6 +21,7 @@ extern "C" const char* fp8_strerror(int code) {
         case FP8_ERR_TIMEOUT: return "device pipeline wait timed out";
         case FP8_ERR_OFFSETS: return "expert offsets or row indices out of range";
         case FP8_ERR_DEVICE: return "no usable sm_100-family device";
+        case FP8_ERR_SCRATCH: return "problem larger than the library's static scratch";
         default: return "unknown status";
     }
 }

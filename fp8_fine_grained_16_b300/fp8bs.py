@@ -33,6 +33,7 @@ FP8_OUT_BF16 = 0
 FP8_OUT_F32 = 1
 FP8_ERR_TIMEOUT = -5
 FP8_ERR_OFFSETS = -6
+FP8_ERR_SCRATCH = -8
 
 _P = ctypes.c_void_p
 _I64 = ctypes.c_int64
@@ -47,6 +48,7 @@ _SIGS = {
     "fp8_gemm_blockscaled": [_P, _P, _P, _P, _I, _P, _I, _I64, _I64, _I64, _P],
     "fp8_grouped_gemm_blockscaled": [_P, _P, _P, _P, _P, _I, _I64, _I64, _I64, _P, _P],
     "fp8_moe_route_topk": [_P, _I64, _I, _I, _P, _P, _P, _P, _P, _P, _P],
+    "fp8_moe_route_topk_noalloc": [_P, _I64, _I, _I, _P, _P, _P, _P, _P, _P],
     "fp8_permute_rows": [_P, _P, _I64, _I64, _P, _I64, _P, _P, _P],
     "fp8_moe_combine_bf16": [_P, _I64, _P, _P, _I64, _I, _I64, _P, _P],
     "fp8_get_status": [_P],
@@ -206,6 +208,23 @@ def fp8_moe_route_topk(logits: torch.Tensor, topk: int, out: dict | None = None,
         _ptr(logits, torch.float32, "logits"), T, E, topk, _ptr(o["idx"], torch.int32), _ptr(o["gate"], torch.float32),
         _ptr(o["off"], torch.int32), _ptr(o["src_row"], torch.int32), _ptr(o["pos"], torch.int32),
         _ptr(work, torch.int32, "work"), _stream(stream)))
+    return o
+
+
+def fp8_moe_route_topk_noalloc(logits: torch.Tensor, topk: int, out: dict | None = None, stream=None) -> dict:
+    """fp8_moe_route_topk for callers that cannot allocate device scratch:
+    the library's own static scratch stands in for `work`.  With `out`
+    given, this call allocates nothing on the device."""
+    T, E = logits.shape
+    dev = logits.device
+    o = out or dict(idx=torch.empty((T, topk), dtype=torch.int32, device=dev),
+                    gate=torch.empty((T, topk), dtype=torch.float32, device=dev),
+                    off=torch.empty(E + 1, dtype=torch.int32, device=dev),
+                    src_row=torch.empty(T * topk, dtype=torch.int32, device=dev),
+                    pos=torch.empty((T, topk), dtype=torch.int32, device=dev))
+    _check("fp8_moe_route_topk_noalloc", lib.fp8_moe_route_topk_noalloc(
+        _ptr(logits, torch.float32, "logits"), T, E, topk, _ptr(o["idx"], torch.int32), _ptr(o["gate"], torch.float32),
+        _ptr(o["off"], torch.int32), _ptr(o["src_row"], torch.int32), _ptr(o["pos"], torch.int32), _stream(stream)))
     return o
 
 

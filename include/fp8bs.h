@@ -60,7 +60,8 @@ enum fp8_status {
     FP8_ERR_CUDA = -4,       /* a CUDA call or launch failed */
     FP8_ERR_TIMEOUT = -5,    /* a kernel's bounded pipeline wait expired (device status) */
     FP8_ERR_OFFSETS = -6,    /* expert offsets not monotone or out of range (device status) */
-    FP8_ERR_DEVICE = -7      /* no usable sm_100-family device */
+    FP8_ERR_DEVICE = -7,     /* no usable sm_100-family device */
+    FP8_ERR_SCRATCH = -8     /* problem larger than the library's static scratch */
 };
 
 /* flags of the quantisers */
@@ -190,6 +191,33 @@ FP8_API int fp8_moe_route_topk(const float* logits, int64_t T, int E, int topk,
                                int32_t* idx, float* gate, int32_t* expert_offsets,
                                int32_t* src_row, int32_t* pos, int32_t* work,
                                fp8_stream_t stream);
+
+/* ------------------------------------------------------------------------
+ * fp8_moe_route_topk without the caller's scratch buffer (the pages have no
+ * counterpart: this is a convenience of the library).  Some callers cannot
+ * allocate device memory where they route: a runtime that gave all of HBM
+ * to its own pool at start-up, or a serving loop that forbids cudaMalloc
+ * after warm-up because allocating can synchronise the device.  This call
+ * takes the same arguments and gives the same results as
+ * fp8_moe_route_topk, minus `work`: its scratch is a fixed device array
+ * inside the library (FP8_ROUTE_NOALLOC_MAX_WORK int32 words, 1 MiB, held
+ * on every GPU that loads the library until the process exits).  It calls no
+ * cudaMalloc or cudaFree.
+ *   - Limit: ceil(T/64) * E <= FP8_ROUTE_NOALLOC_MAX_WORK (for E = 256,
+ *     T <= 65536); larger problems return FP8_ERR_SCRATCH and launch
+ *     nothing.
+ *   - The first call on a device looks up the array's device address
+ *     (cudaGetSymbolAddress, with that device current) and caches it; make
+ *     that first call before any stream capture.
+ *   - Every call uses the same array and leaves its last contents there
+ *     (nothing in it needs clearing: each call writes every word it reads).
+ *     Calls whose kernels overlap on the GPU, e.g. on two streams at once,
+ *     race on it and give wrong routes: serialise them.
+ * ---------------------------------------------------------------------- */
+#define FP8_ROUTE_NOALLOC_MAX_WORK (1 << 18)
+FP8_API int fp8_moe_route_topk_noalloc(const float* logits, int64_t T, int E, int topk,
+                                       int32_t* idx, float* gate, int32_t* expert_offsets,
+                                       int32_t* src_row, int32_t* pos, fp8_stream_t stream);
 
 /* ------------------------------------------------------------------------
  * Dispatch on one GPU: gather FP8 rows and their scales (page 4: activations
