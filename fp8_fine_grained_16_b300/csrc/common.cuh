@@ -90,11 +90,43 @@ FP8_DEV bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
     return ok != 0;
 }
 
+// Non-blocking probe of the phase (much cheaper than try_wait when the
+// phase has already completed).
+FP8_DEV bool mbar_test_wait(uint64_t* bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+// Probe two barriers at once: both tests are in flight together, so the
+// pair costs about one probe.  True when both phases have completed.
+FP8_DEV bool mbar_test_wait2(uint64_t* b0, uint32_t p0, uint64_t* b1, uint32_t p1) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred a, b;\n\t"
+        "mbarrier.test_wait.parity.shared::cta.b64 a, [%1], %2;\n\t"
+        "mbarrier.test_wait.parity.shared::cta.b64 b, [%3], %4;\n\t"
+        "and.pred a, a, b;\n\t"
+        "selp.u32 %0, 1, 0, a;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(b0)), "r"(p0), "r"(smem_u32(b1)), "r"(p1)
+        : "memory");
+    return ok != 0;
+}
+
 // Wait for the phase of `bar` with the given parity, giving up after
 // timeout_ns or as soon as *abort becomes non-zero.  On a timeout the waiter
-// raises *abort itself.  Returns true when the phase completed.
+// raises *abort itself.  Returns true when the phase completed.  A phase that
+// is already complete is caught by the non-blocking probe first.
 FP8_DEV bool mbar_wait_bounded(uint64_t* bar, uint32_t parity, volatile int* abort,
                                uint64_t timeout_ns = kWaitTimeoutNs) {
+    if (mbar_test_wait(bar, parity)) return true;
     if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = globaltimer_ns();
     for (uint32_t i = 1;; ++i) {
@@ -112,6 +144,13 @@ FP8_DEV bool mbar_wait_bounded(uint64_t* bar, uint32_t parity, volatile int* abo
 // ---------------------------------------------------------------- TMA
 FP8_DEV void tma_prefetch_desc(const CUtensorMap* map) {
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
+}
+FP8_DEV void tma_load_1d(void* dst, const CUtensorMap* map, uint64_t* bar, int32_t c0) {
+    asm volatile(
+        "cp.async.bulk.tensor.1d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%3}], [%2];" ::"r"(
+            smem_u32(dst)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(c0)
+        : "memory");
 }
 FP8_DEV void tma_load_2d(void* dst, const CUtensorMap* map, uint64_t* bar, int32_t c0, int32_t c1) {
     asm volatile(
@@ -171,6 +210,31 @@ FP8_DEV void tmem_ld_32x32b_x32(uint32_t taddr, uint32_t (&v)[32]) {
         : "memory");
 }
 FP8_DEV void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+
+// Compiler-only fence: the registers in v are treated as modified here, so
+// their uses cannot move above this point (placed right after a
+// tcgen05.wait::ld that covers the load that wrote them).
+FP8_DEV void regs_fence(uint32_t (&v)[32]) {
+    asm volatile(""
+                 : "+r"(v[0]), "+r"(v[1]), "+r"(v[2]), "+r"(v[3]), "+r"(v[4]), "+r"(v[5]), "+r"(v[6]), "+r"(v[7]),
+                   "+r"(v[8]), "+r"(v[9]), "+r"(v[10]), "+r"(v[11]), "+r"(v[12]), "+r"(v[13]), "+r"(v[14]),
+                   "+r"(v[15]), "+r"(v[16]), "+r"(v[17]), "+r"(v[18]), "+r"(v[19]), "+r"(v[20]), "+r"(v[21]),
+                   "+r"(v[22]), "+r"(v[23]), "+r"(v[24]), "+r"(v[25]), "+r"(v[26]), "+r"(v[27]), "+r"(v[28]),
+                   "+r"(v[29]), "+r"(v[30]), "+r"(v[31]));
+}
+
+// tcgen05.wait::ld that also names the registers a preceding tcgen05.ld
+// wrote, so that the compiler cannot move their uses above the wait.
+FP8_DEV void tmem_wait_ld_regs(uint32_t (&v)[32]) {
+    asm volatile(
+        "tcgen05.wait::ld.sync.aligned;"
+        : "+r"(v[0]), "+r"(v[1]), "+r"(v[2]), "+r"(v[3]), "+r"(v[4]), "+r"(v[5]), "+r"(v[6]), "+r"(v[7]),
+          "+r"(v[8]), "+r"(v[9]), "+r"(v[10]), "+r"(v[11]), "+r"(v[12]), "+r"(v[13]), "+r"(v[14]), "+r"(v[15]),
+          "+r"(v[16]), "+r"(v[17]), "+r"(v[18]), "+r"(v[19]), "+r"(v[20]), "+r"(v[21]), "+r"(v[22]), "+r"(v[23]),
+          "+r"(v[24]), "+r"(v[25]), "+r"(v[26]), "+r"(v[27]), "+r"(v[28]), "+r"(v[29]), "+r"(v[30]), "+r"(v[31])
+        :
+        : "memory");
+}
 
 // Shared-memory matrix descriptor for a K-major operand tile stored as rows
 // of 128 bytes with the 128-byte swizzle (the layout a TMA load with

@@ -8,22 +8,31 @@
 //   P_kb    = A[:, 128kb : 128kb+128] * B[:, 128kb : 128kb+128]^T   (E4M3 MMA)
 //
 // The pages' Hopper scheme overlaps promotion with WGMMA by ping-ponging two
-// warpgroups.  Here the overlap comes from tensor memory instead:
+// warpgroups.  Here the overlap comes from tensor memory instead.  One CTA
+// per SM computes 128 x 256 output tiles:
 //
-//   warp 0        TMA producer: A (128 x 128 B) and B (BN x 128 B) tiles of
-//                 one K block per pipeline stage, 128-byte swizzle.
-//   warp 1        allocates TMEM and issues, per K block, four
-//                 tcgen05.mma (K = 32 each) into one of two TMEM
-//                 accumulators (BN fp32 columns each), then commits to the
-//                 stage's "empty" barrier and the accumulator's "full"
-//                 barrier.
+//   warp 0        TMA producer.  Per K block one pipeline stage receives the
+//                 A tile (128 x 128 B), the B tile (256 x 128 B), both with
+//                 the 128-byte swizzle, and the scales the promotion needs:
+//                 sA of the tile's 128 rows and sB of its columns.
+//   warp 1        allocates TMEM and issues, per K block, four tcgen05.mma
+//                 (K = 32 each) into one of two TMEM accumulators (256 fp32
+//                 columns each), then commits to the stage's "empty" barrier
+//                 and the accumulator's "full" barrier.
 //   warps 2, 3    idle (they only give their registers to the promotion warps)
-//   warps 4..11   promotion: two warpgroups, one per half of the BN columns.
-//                 Thread (warp w, lane l) owns tile row 32*(w%4)+l (TMEM
-//                 lanes are tied to w%4).  Per K block it reads P_kb from
-//                 TMEM, frees the accumulator, and adds P_kb * sA*sB into
-//                 BN/2 fp32 registers.  While it does so the MMA warp is
-//                 already filling the other accumulator with P_{kb+1}.
+//   warps 4..11   promotion: two warpgroups, one per 128-column half.  Thread
+//                 (warp w, lane l) owns tile row 32*(w%4)+l (TMEM lanes are
+//                 tied to w%4).  Per K block it reads P_kb from TMEM in two
+//                 64-column batches, frees the accumulator (one arrive per
+//                 warp) as soon as the second batch is in registers, and adds
+//                 P_kb * sA*sB into 128 fp32 registers with packed two-lane
+//                 FMAs.  Meanwhile the MMA warp already fills the other
+//                 accumulator with P_{kb+1}.  A stage is refilled only after
+//                 the MMAs and all eight promotion warps are done with it.
+//
+// An mbarrier probe costs a couple of hundred cycles on this part even when
+// the phase has completed, so each role tests the two barriers it needs per
+// K block in one combined probe.
 //
 // The kernel is persistent: one CTA per SM walks a static list of output
 // tiles; stage and accumulator indices run on across tile boundaries, so the
@@ -47,27 +56,42 @@ constexpr int BM = 128;                 // tile rows (one tcgen05 M=128 MMA)
 constexpr int BK = 128;                 // K block = promotion interval = scale block
 constexpr int kThreads = 384;           // 12 warps = 3 warpgroups
 constexpr int kPromoThreads = 256;      // warps 4..11
+constexpr int kPromoWarps = kPromoThreads / 32;
 // Register split: the block launches with 168 registers per thread (384 x 168
 // = 64512); warpgroup 0 (TMA, MMA, idle) gives back down to 40 and the two
 // promotion warpgroups grow to 232: 128*40 + 256*232 = 64512.
 constexpr int kTmemCols = 512;
 constexpr int kMaxExperts = 1024;
+// Scales travel in the pipeline stage through rank-1 TMA maps.  A tensor
+// copy starts on a 16-byte boundary of global memory, so the sA box
+// (kSaBox floats) starts at the tile's first row rounded down to a multiple
+// of 4 elements and the promotion indexes past that offset; each box lands
+// on a 128-byte boundary of shared memory.
+constexpr int kSaBox = BM + 4;                   // 132 floats = 528 bytes
+constexpr int kSaRegion = 640;                   // bytes reserved for it in a stage
+constexpr int kSbBox0 = 4;                       // BMODE 0: 16-byte box around one block scale
+constexpr int kSbHalf0 = 32;                     // BMODE 0: floats between the two halves' boxes (128 bytes)
+static_assert(kSaRegion % 128 == 0 && kSaRegion >= kSaBox * 4 && (kSbHalf0 * 4) % 128 == 0, "TMA box alignment");
 
 template <int BN, int STAGES, int BMODE, bool GROUPED>
 struct Layout {
     static constexpr int kABytes = BM * BK;
     static constexpr int kBBytes = BN * BK;
-    static constexpr int kStageBytes = kABytes + kBBytes;
+    static constexpr int kSaOff = kABytes + kBBytes;                        // in a stage
+    static constexpr int kSbOff = kSaOff + kSaRegion;
+    static constexpr int kSbRegion = BMODE == 1 ? BN * 4 : 2 * kSbHalf0 * 4;
+    static constexpr int kStageBytes = (kSbOff + kSbRegion + 1023) & ~1023;
+    static constexpr uint32_t kTxBytes = kABytes + kBBytes + kSaBox * 4 + (BMODE == 1 ? BN * 4 : 2 * kSbBox0 * 4);
     static constexpr int kStagesBytes = STAGES * kStageBytes;
-    static constexpr int kBarOff = kStagesBytes;  // full[S], empty[S], tfull[2], tempty[2], done, sbar[2][2]
-    static constexpr int kNumBars = 2 * STAGES + 9;
+    static constexpr int kBarOff = kStagesBytes;  // full[S], empty[S], tfull[2], tempty[2], done
+    static constexpr int kNumBars = 2 * STAGES + 5;
     static constexpr int kMiscOff = kBarOff + kNumBars * 8;       // tmem base, abort flag
-    static constexpr int kSbOff = (kMiscOff + 16 + 15) & ~15;     // row-scale buffers [2][BN] (BMODE 1)
-    static constexpr int kSbBytes = BMODE == 1 ? 2 * BN * 4 : 0;
-    static constexpr int kGrpOff = kSbOff + kSbBytes;             // grouped: off[E+1], tile prefix[E+1]
+    static constexpr int kGrpOff = (kMiscOff + 16 + 15) & ~15;    // grouped: off[E+1], tile prefix[E+1]
     static constexpr int kGrpBytes = GROUPED ? 2 * (kMaxExperts + 1) * 4 : 0;
     static constexpr int kBytes = kGrpOff + kGrpBytes;
     static constexpr int kDynSmem = kBytes + 1024;                // slack for 1024-byte alignment
+    static_assert(kABytes % 1024 == 0 && kStageBytes % 1024 == 0, "operand tiles start on 1024-byte boundaries");
+    static_assert(kSaOff % 128 == 0 && kSbOff % 128 == 0, "scale boxes start on 128-byte boundaries");
 };
 
 struct GemmArgs {
@@ -137,14 +161,13 @@ struct GroupedSched {
 template <int BN, int STAGES, int BMODE, bool OUT_F32, bool GROUPED>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_blockscaled_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                            const __grid_constant__ CUtensorMap tmSA, const __grid_constant__ CUtensorMap tmSB,
                             const GemmArgs args) {
     using L = Layout<BN, STAGES, BMODE, GROUPED>;
     static_assert(2 * BN <= kTmemCols, "two accumulators must fit in TMEM");
     static_assert(BN == 256, "one promotion half = 128 columns = one scale block and one column per warpgroup thread");
     constexpr int kHalf = BN / 2;          // columns per promotion warpgroup
-    constexpr int kChunks = kHalf / 32;
     constexpr uint32_t kIdesc = idesc_e4m3_f32(BM, BN);
-    constexpr uint32_t kTxBytes = L::kABytes + L::kBBytes;
 
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -154,7 +177,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint64_t* tfull = bars + 2 * STAGES;
     uint64_t* tempty = bars + 2 * STAGES + 2;
     uint64_t* done = bars + 2 * STAGES + 4;
-    uint64_t* sbar = bars + 2 * STAGES + 5;      // row-scale buffer barriers [half][buffer] (BMODE 1)
     uint32_t* tmem_base_s = reinterpret_cast<uint32_t*>(smem + L::kMiscOff);
     volatile int* abort_s = reinterpret_cast<volatile int*>(smem + L::kMiscOff + 4);
 
@@ -166,20 +188,21 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (threadIdx.x == 0) {
         for (int i = 0; i < STAGES; ++i) {
             mbar_init(&full[i], 1);
-            mbar_init(&empty[i], 1);
+            mbar_init(&empty[i], 1 + kPromoWarps);          // MMA commit + every promotion warp
         }
         for (int i = 0; i < 2; ++i) {
             mbar_init(&tfull[i], 1);
-            mbar_init(&tempty[i], kPromoThreads);
+            mbar_init(&tempty[i], kPromoWarps);             // one arrive per promotion warp
         }
         mbar_init(done, 1);
-        for (int i = 0; i < 4; ++i) mbar_init(&sbar[i], 128);
         *abort_s = 0;
         fence_mbar_init();
     }
     if (warp == 0 && lane == 0) {
         tma_prefetch_desc(&tmA);
         tma_prefetch_desc(&tmB);
+        tma_prefetch_desc(&tmSA);
+        tma_prefetch_desc(&tmSB);
     }
     if (warp == 1) {
         tmem_alloc(tmem_base_s, kTmemCols);
@@ -238,6 +261,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     };
     int64_t num_tiles;
     if constexpr (GROUPED) num_tiles = gs.count(); else num_tiles = ds.count();
+    // BMODE 0: index in sb of K block 0 of the 128x128 block scales of column
+    // half h of tile t (a half past N reads an in-bounds scale, never stored)
+    auto sb_row = [&](const Tile& t, int h) -> int64_t {
+        const int64_t c0 = int64_t(t.n0) + h * kHalf;
+        return (int64_t(t.e) * (args.N / 128) + (c0 < args.N ? c0 : args.N - 1) / 128) * nkb;
+    };
 
     if (warp < 4) {
         asm volatile("setmaxnreg.dec.sync.aligned.u32 40;");
@@ -248,20 +277,32 @@ __global__ void __launch_bounds__(kThreads, 1)
                 bool ok = true;
                 for (int64_t w = blockIdx.x; ok && w < num_tiles; w += gridDim.x) {
                     const Tile t = tile_at(w);
+                    int64_t sbr[2] = {0, 0};
+                    if constexpr (BMODE == 0) {
+                        sbr[0] = sb_row(t, 0);
+                        sbr[1] = sb_row(t, 1);
+                    }
                     for (int64_t kb = 0; kb < nkb; ++kb) {
                         const uint32_t stage = it % STAGES, phase = (it / STAGES) & 1u;
                         if (!mbar_wait_bounded(&empty[stage], phase ^ 1u, abort_s)) {
                             ok = false;
                             break;
                         }
-                        uint8_t* sa_tile = smem + stage * L::kStageBytes;
-                        uint8_t* sb_tile = sa_tile + L::kABytes;
-                        mbar_arrive_expect_tx(&full[stage], kTxBytes);
-                        tma_load_2d(sa_tile, &tmA, &full[stage], int32_t(kb * BK), int32_t(t.row0));
+                        uint8_t* st = smem + stage * L::kStageBytes;
+                        mbar_arrive_expect_tx(&full[stage], L::kTxBytes);
+                        tma_load_2d(st, &tmA, &full[stage], int32_t(kb * BK), int32_t(t.row0));
                         if constexpr (GROUPED)
-                            tma_load_3d(sb_tile, &tmB, &full[stage], int32_t(kb * BK), t.n0, t.e);
+                            tma_load_3d(st + L::kABytes, &tmB, &full[stage], int32_t(kb * BK), t.n0, t.e);
                         else
-                            tma_load_2d(sb_tile, &tmB, &full[stage], int32_t(kb * BK), t.n0);
+                            tma_load_2d(st + L::kABytes, &tmB, &full[stage], int32_t(kb * BK), t.n0);
+                        tma_load_1d(st + L::kSaOff, &tmSA, &full[stage], int32_t((kb * args.M + t.row0) & ~int64_t(3)));
+                        if constexpr (BMODE == 0) {
+                            tma_load_1d(st + L::kSbOff, &tmSB, &full[stage], int32_t((sbr[0] + kb) & ~int64_t(3)));
+                            tma_load_1d(st + L::kSbOff + kSbHalf0 * 4, &tmSB, &full[stage],
+                                        int32_t((sbr[1] + kb) & ~int64_t(3)));
+                        } else {
+                            tma_load_1d(st + L::kSbOff, &tmSB, &full[stage], int32_t(kb * args.N + t.n0));
+                        }
                         ++it;
                     }
                 }
@@ -274,6 +315,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (uint32_t j = first; j < it; ++j)
                     mbar_wait_bounded(&full[j % STAGES], (j / STAGES) & 1u, reinterpret_cast<volatile int*>(&zero));
             }
+            __syncwarp();
         } else if (warp == 1) {
             // ================= MMA issuer
             if (lane == 0) {
@@ -282,10 +324,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int64_t w = blockIdx.x; ok && w < num_tiles; w += gridDim.x) {
                     for (int64_t kb = 0; kb < nkb; ++kb) {
                         const uint32_t buf = g & 1u, tphase = (g >> 1) & 1u;
-                        if (!mbar_wait_bounded(&tempty[buf], tphase ^ 1u, abort_s)) { ok = false; break; }
-                        tc_fence_after();
                         const uint32_t stage = it % STAGES, phase = (it / STAGES) & 1u;
-                        if (!mbar_wait_bounded(&full[stage], phase, abort_s)) { ok = false; break; }
+                        // the stage is usually loaded long before the accumulator frees up
+                        if (!mbar_test_wait2(&full[stage], phase, &tempty[buf], tphase ^ 1u)) {
+                            if (!mbar_wait_bounded(&full[stage], phase, abort_s)) { ok = false; break; }
+                            if (!mbar_wait_bounded(&tempty[buf], tphase ^ 1u, abort_s)) { ok = false; break; }
+                        }
                         tc_fence_after();
                         const uint32_t a_addr = smem_u32(smem + stage * L::kStageBytes);
                         const uint32_t b_addr = a_addr + L::kABytes;
@@ -316,79 +360,101 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int half = (warp - 4) >> 2;              // 0: columns [0, BN/2), 1: [BN/2, BN)
         const int r = wq * 32 + lane;                  // tile row
         const uint32_t t_lane = uint32_t(wq * 32) << 16;
-        float* sbuf = reinterpret_cast<float*>(smem + L::kSbOff);   // [2][BN], BMODE 1
-        const int wg_tid = threadIdx.x - 128 - half * 128;          // 0..127 within the warpgroup
+
         uint32_t g = 0;
         bool ok = true;
         for (int64_t w = blockIdx.x; ok && w < num_tiles; w += gridDim.x) {
             const Tile t = tile_at(w);
             const int64_t m = t.row0 + r;
-            const int64_t m_ld = m < args.M ? m : args.M - 1;     // in-bounds row for scale loads
             const int64_t ncol0 = int64_t(t.n0) + half * kHalf;   // first column of this thread's half
             // N % 128 == 0, so a half tile (128 columns) is either entirely
             // inside [0, N) or entirely past it (last tile of an N that is an
-            // odd multiple of 128); a half past N loads in-bounds scales and
-            // stores nothing.
+            // odd multiple of 128).
             const bool cols_ok = ncol0 < args.N;
-            const int64_t ncol_ld = cols_ok ? ncol0 : args.N - kHalf;
-            const float* sb_e = args.sb;
-            if constexpr (GROUPED) sb_e += int64_t(t.e) * (args.N / 128) * nkb;
+            const int64_t sbr = BMODE == 0 ? sb_row(t, half) : 0;
 
-            auto load_sa = [&](int64_t kb) { return __ldg(args.sa + kb * args.M + m_ld); };
-            auto load_sb = [&](int64_t kb) -> float {
-                if constexpr (BMODE == 0) return __ldg(sb_e + (ncol_ld / 128) * nkb + kb);
-                else return __ldg(sb_e + kb * args.N + ncol_ld + wg_tid);
-            };
-
-            float acc[kHalf];
+            float2 acc[kHalf / 2];
 #pragma unroll
-            for (int i = 0; i < kHalf; ++i) acc[i] = 0.0f;
-            float sa_next = load_sa(0), sb_next = load_sb(0);
+            for (int i = 0; i < kHalf / 2; ++i) acc[i] = make_float2(0.0f, 0.0f);
 
             for (int64_t kb = 0; kb < nkb; ++kb) {
-                const float sa_cur = sa_next, sb_cur = sb_next;
-                if (kb + 1 < nkb) {
-                    sa_next = load_sa(kb + 1);
-                    sb_next = load_sb(kb + 1);
-                }
+                const uint32_t stage = g % STAGES, phase = (g / STAGES) & 1u;
                 const uint32_t buf = g & 1u, tphase = (g >> 1) & 1u;
-                if constexpr (BMODE == 1) {
-                    // publish this K block's column scales to the warpgroup (double-buffered;
-                    // a buffer is rewritten two blocks later, after every thread of the
-                    // warpgroup has arrived on the next block's barrier)
-                    sbuf[buf * BN + half * kHalf + wg_tid] = sb_cur;
-                    mbar_arrive(&sbar[half * 2 + buf]);
-                    if (!mbar_wait_bounded(&sbar[half * 2 + buf], tphase, abort_s)) { ok = false; break; }
-                }
-                if (!mbar_wait_bounded(&tfull[buf], tphase, abort_s)) { ok = false; break; }
+                // Lane 0 waits for this K block's stage (its scales) and
+                // accumulator; __syncwarp passes the acquire on to the other
+                // lanes, and the warp leaves the loop as a whole if a wait
+                // gave up (the tcgen05 loads below are warp-collective).
+                bool got = true;
+                if (lane == 0 && !mbar_test_wait2(&full[stage], phase, &tfull[buf], tphase))
+                    got = mbar_wait_bounded(&full[stage], phase, abort_s) &&
+                          mbar_wait_bounded(&tfull[buf], tphase, abort_s);
+                got = __shfl_sync(0xFFFFFFFFu, got ? 1 : 0, 0) != 0;
+                __syncwarp();
+                if (!got) { ok = false; break; }
                 tc_fence_after();
-                const uint32_t tcol = tmem_base + t_lane + buf * BN + half * kHalf;
-#pragma unroll
-                for (int c = 0; c < kChunks; ++c) {
-                    uint32_t v[32];
-                    tmem_ld_32x32b_x32(tcol + c * 32, v);
-                    tmem_wait_ld();
-                    if (c == kChunks - 1) {
-                        tc_fence_before();
-                        mbar_arrive(&tempty[buf]);           // accumulator may be overwritten now
-                    }
+
+                const uint8_t* st = smem + stage * L::kStageBytes;
+                // the sA box starts at (kb*M + row0) rounded down to 4 elements
+                const float sa_cur = reinterpret_cast<const float*>(st + L::kSaOff)[int((kb * args.M + t.row0) & 3) + r];
+                const float2 sa2 = make_float2(sa_cur, sa_cur);
+                float2 sc2 = sa2;
+                const float* sbk = reinterpret_cast<const float*>(st + L::kSbOff) + half * kHalf;   // BMODE 1
+                if constexpr (BMODE == 0) {
+                    const float sbv =
+                        reinterpret_cast<const float*>(st + L::kSbOff)[half * kSbHalf0 + int((sbr + kb) & 3)];
+                    const float sc = __fmul_rn(sa_cur, sbv);
+                    sc2 = make_float2(sc, sc);
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&empty[stage]);      // this warp is done with the stage
+                }
+
+                auto scale_chunk = [&](int c, const uint32_t (&v)[32]) {
                     if constexpr (BMODE == 0) {
-                        const float sc = __fmul_rn(sa_cur, sb_cur);
 #pragma unroll
-                        for (int i = 0; i < 32; ++i) acc[c * 32 + i] = fmaf(__uint_as_float(v[i]), sc, acc[c * 32 + i]);
+                        for (int i = 0; i < 16; ++i)
+                            acc[c * 16 + i] = __ffma2_rn(
+                                make_float2(__uint_as_float(v[2 * i]), __uint_as_float(v[2 * i + 1])), sc2,
+                                acc[c * 16 + i]);
                     } else {
-                        const float4* sbv = reinterpret_cast<const float4*>(sbuf + buf * BN + half * kHalf + c * 32);
+                        const float4* sbv = reinterpret_cast<const float4*>(sbk + c * 32);
 #pragma unroll
                         for (int i4 = 0; i4 < 8; ++i4) {
                             const float4 b4 = sbv[i4];
-                            const float bs[4] = {b4.x, b4.y, b4.z, b4.w};
-#pragma unroll
-                            for (int j = 0; j < 4; ++j) {
-                                const int i = i4 * 4 + j;
-                                acc[c * 32 + i] = fmaf(__uint_as_float(v[i]), __fmul_rn(sa_cur, bs[j]), acc[c * 32 + i]);
-                            }
+                            const float2 p0 = __fmul2_rn(
+                                make_float2(__uint_as_float(v[4 * i4]), __uint_as_float(v[4 * i4 + 1])),
+                                make_float2(b4.x, b4.y));
+                            const float2 p1 = __fmul2_rn(
+                                make_float2(__uint_as_float(v[4 * i4 + 2]), __uint_as_float(v[4 * i4 + 3])),
+                                make_float2(b4.z, b4.w));
+                            acc[c * 16 + 2 * i4] = __ffma2_rn(p0, sa2, acc[c * 16 + 2 * i4]);
+                            acc[c * 16 + 2 * i4 + 1] = __ffma2_rn(p1, sa2, acc[c * 16 + 2 * i4 + 1]);
                         }
                     }
+                };
+
+                const uint32_t tcol = tmem_base + t_lane + buf * BN + half * kHalf;
+                uint32_t va[32], vb[32];
+                // columns [0, 64) of this half
+                tmem_ld_32x32b_x32(tcol, va);
+                tmem_ld_32x32b_x32(tcol + 32, vb);
+                tmem_wait_ld_regs(va);
+                regs_fence(vb);
+                scale_chunk(0, va);
+                scale_chunk(1, vb);
+                // columns [64, 128); once they are in registers the accumulator
+                // is free for the MMAs two K blocks ahead
+                tmem_ld_32x32b_x32(tcol + 64, va);
+                tmem_ld_32x32b_x32(tcol + 96, vb);
+                tmem_wait_ld_regs(va);
+                regs_fence(vb);
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&tempty[buf]);
+                scale_chunk(2, va);
+                scale_chunk(3, vb);
+                if constexpr (BMODE == 1) {
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&empty[stage]);      // column scales no longer read
                 }
                 ++g;
             }
@@ -399,16 +465,17 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if constexpr (OUT_F32) {
                     float* dst = reinterpret_cast<float*>(args.d) + m * args.N + ncol0;
 #pragma unroll
-                    for (int i = 0; i < kHalf; i += 4)
-                        *reinterpret_cast<float4*>(dst + i) = make_float4(acc[i], acc[i + 1], acc[i + 2], acc[i + 3]);
+                    for (int i = 0; i < kHalf / 2; i += 2)
+                        *reinterpret_cast<float4*>(dst + 2 * i) =
+                            make_float4(acc[i].x, acc[i].y, acc[i + 1].x, acc[i + 1].y);
                 } else {
                     uint16_t* dst = reinterpret_cast<uint16_t*>(args.d) + m * args.N + ncol0;
 #pragma unroll
-                    for (int i = 0; i < kHalf; i += 8) {
-                        const uint4 o = make_uint4(cvt_bf16x2(acc[i], acc[i + 1]), cvt_bf16x2(acc[i + 2], acc[i + 3]),
-                                                   cvt_bf16x2(acc[i + 4], acc[i + 5]),
-                                                   cvt_bf16x2(acc[i + 6], acc[i + 7]));
-                        *reinterpret_cast<uint4*>(dst + i) = o;
+                    for (int i = 0; i < kHalf / 2; i += 4) {
+                        const uint4 o = make_uint4(cvt_bf16x2(acc[i].x, acc[i].y), cvt_bf16x2(acc[i + 1].x, acc[i + 1].y),
+                                                   cvt_bf16x2(acc[i + 2].x, acc[i + 2].y),
+                                                   cvt_bf16x2(acc[i + 3].x, acc[i + 3].y));
+                        *reinterpret_cast<uint4*>(dst + 2 * i) = o;
                     }
                 }
             }
@@ -457,6 +524,21 @@ static bool make_operand_map(CUtensorMap* map, const void* base, int64_t rows, i
     return r == CUDA_SUCCESS;
 }
 
+// Rank-1 fp32 view of a scale tensor of n elements, box of `box` floats, no
+// swizzle, zero fill past the end.
+static bool make_scale_map(CUtensorMap* map, const float* base, int64_t n, int box) {
+    auto fn = encode_fn();
+    if (!fn) return false;
+    cuuint64_t dims[1] = {cuuint64_t(n)};
+    cuuint64_t strides[1] = {0};
+    cuuint32_t boxd[1] = {cuuint32_t(box)};
+    cuuint32_t estr[1] = {1u};
+    CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 1u, const_cast<float*>(base), dims, strides, boxd, estr,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
 static int device_sms() {
     int dev = 0, n = 0, major = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return -1;
@@ -466,7 +548,8 @@ static int device_sms() {
 }
 
 template <int BN, int STAGES, int BMODE, bool OUT_F32, bool GROUPED>
-static int launch(const CUtensorMap& ma, const CUtensorMap& mb, const GemmArgs& args, int grid, cudaStream_t stream) {
+static int launch(const CUtensorMap& ma, const CUtensorMap& mb, const CUtensorMap& msa, const CUtensorMap& msb,
+                  const GemmArgs& args, int grid, cudaStream_t stream) {
     using L = Layout<BN, STAGES, BMODE, GROUPED>;
     auto kern = gemm_blockscaled_kernel<BN, STAGES, BMODE, OUT_F32, GROUPED>;
     static bool attr_set = false;
@@ -475,7 +558,7 @@ static int launch(const CUtensorMap& ma, const CUtensorMap& mb, const GemmArgs& 
             return FP8_ERR_CUDA;
         attr_set = true;
     }
-    kern<<<grid, kThreads, L::kDynSmem, stream>>>(ma, mb, args);
+    kern<<<grid, kThreads, L::kDynSmem, stream>>>(ma, mb, msa, msb, args);
     return cudaGetLastError() == cudaSuccess ? FP8_OK : FP8_ERR_CUDA;
 }
 
@@ -509,24 +592,27 @@ extern "C" int fp8_gemm_blockscaled(const uint8_t* a, const float* sa, const uin
         return FP8_ERR_ARG;
     if (K % 128 || N % 128) return FP8_ERR_SHAPE;
     if (M > (int64_t(1) << 31) - 1 || N > (int64_t(1) << 31) - 1 || K > (int64_t(1) << 31) - 1) return FP8_ERR_SHAPE;
-    if (!aligned16(a) || !aligned16(b) || !aligned16(d) || (reinterpret_cast<uintptr_t>(sa) & 3u) ||
-        !aligned16(sb))
-        return FP8_ERR_ALIGN;
+    if (!aligned16(a) || !aligned16(b) || !aligned16(d) || !aligned16(sa) || !aligned16(sb)) return FP8_ERR_ALIGN;
+    if (M * (K / 128) >= (int64_t(1) << 31) || (b_scale_mode == FP8_BSCALE_ROW && N * (K / 128) >= (int64_t(1) << 31)))
+        return FP8_ERR_SHAPE;
     const int sms = device_sms();
     if (sms <= 0) return FP8_ERR_DEVICE;
-    CUtensorMap ma, mb;
-    if (!make_operand_map(&ma, a, M, K, BM, 1, false) || !make_operand_map(&mb, b, N, K, kBN, 1, false))
+    CUtensorMap ma, mb, msa, msb;
+    const int64_t nsb = b_scale_mode == FP8_BSCALE_ROW ? N * (K / 128) : (N / 128) * (K / 128);
+    if (!make_operand_map(&ma, a, M, K, BM, 1, false) || !make_operand_map(&mb, b, N, K, kBN, 1, false) ||
+        !make_scale_map(&msa, sa, M * (K / 128), kSaBox) ||
+        !make_scale_map(&msb, sb, nsb, b_scale_mode == FP8_BSCALE_ROW ? kBN : kSbBox0))
         return FP8_ERR_CUDA;
     GemmArgs args{sa, sb, d, nullptr, M, N, K, 0};
     const int64_t tiles = ((M + BM - 1) / BM) * ((N + kBN - 1) / kBN);
     const int grid = int(tiles < sms ? tiles : sms);
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     if (b_scale_mode == FP8_BSCALE_BLOCK128) {
-        if (d_dtype == FP8_OUT_BF16) return launch<kBN, kStages, 0, false, false>(ma, mb, args, grid, s);
-        return launch<kBN, kStages, 0, true, false>(ma, mb, args, grid, s);
+        if (d_dtype == FP8_OUT_BF16) return launch<kBN, kStages, 0, false, false>(ma, mb, msa, msb, args, grid, s);
+        return launch<kBN, kStages, 0, true, false>(ma, mb, msa, msb, args, grid, s);
     }
-    if (d_dtype == FP8_OUT_BF16) return launch<kBN, kStages, 1, false, false>(ma, mb, args, grid, s);
-    return launch<kBN, kStages, 1, true, false>(ma, mb, args, grid, s);
+    if (d_dtype == FP8_OUT_BF16) return launch<kBN, kStages, 1, false, false>(ma, mb, msa, msb, args, grid, s);
+    return launch<kBN, kStages, 1, true, false>(ma, mb, msa, msb, args, grid, s);
 }
 
 extern "C" int fp8_grouped_gemm_blockscaled(const uint8_t* a, const float* sa, const uint8_t* b, const float* sb,
@@ -539,16 +625,20 @@ extern "C" int fp8_grouped_gemm_blockscaled(const uint8_t* a, const float* sa, c
         return FP8_ERR_SHAPE;
     if (total_rows == 0) return FP8_OK;
     if (!a || !sa || !d) return FP8_ERR_ARG;
-    if (!aligned16(a) || !aligned16(b) || !aligned16(d) || (reinterpret_cast<uintptr_t>(sa) & 3u) ||
-        (reinterpret_cast<uintptr_t>(sb) & 3u) || (reinterpret_cast<uintptr_t>(expert_offsets) & 3u))
+    if (!aligned16(a) || !aligned16(b) || !aligned16(d) || !aligned16(sa) || !aligned16(sb) ||
+        (reinterpret_cast<uintptr_t>(expert_offsets) & 3u))
         return FP8_ERR_ALIGN;
+    if (total_rows * (K / 128) >= (int64_t(1) << 31) || int64_t(E) * (N / 128) * (K / 128) >= (int64_t(1) << 31))
+        return FP8_ERR_SHAPE;
     const int sms = device_sms();
     if (sms <= 0) return FP8_ERR_DEVICE;
-    CUtensorMap ma, mb;
-    if (!make_operand_map(&ma, a, total_rows, K, BM, 1, false) || !make_operand_map(&mb, b, N, K, kBN, E, true))
+    CUtensorMap ma, mb, msa, msb;
+    if (!make_operand_map(&ma, a, total_rows, K, BM, 1, false) || !make_operand_map(&mb, b, N, K, kBN, E, true) ||
+        !make_scale_map(&msa, sa, total_rows * (K / 128), kSaBox) ||
+        !make_scale_map(&msb, sb, int64_t(E) * (N / 128) * (K / 128), kSbBox0))
         return FP8_ERR_CUDA;
     GemmArgs args{sa, sb, d, expert_offsets, total_rows, N, K, E};
-    return launch<kBN, kStages, 0, false, true>(ma, mb, args, sms, reinterpret_cast<cudaStream_t>(stream));
+    return launch<kBN, kStages, 0, false, true>(ma, mb, msa, msb, args, sms, reinterpret_cast<cudaStream_t>(stream));
 }
 
 extern "C" int fp8_selftest_wait_timeout(uint64_t timeout_ns, fp8_stream_t stream) {
