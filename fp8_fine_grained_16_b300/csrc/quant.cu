@@ -30,39 +30,38 @@ __global__ void __launch_bounds__(256) cast_e4m3_kernel(const float* __restrict_
 }
 
 // ------------------------------------------------------------------ 1x128
-// A half-warp owns one tile: lane l of the half holds elements [8l, 8l+8).
-// A warp therefore quantises two tiles per step; the grid strides over tile
-// pairs so that both halves of a warp always run the same loop trip count
-// (the shuffles need the whole warp).  Tiles are numbered row-major
-// (tile = m * nkb + kb), which follows the memory order of x.
+// One warp per row; a half-warp owns one tile (lane l of the half holds
+// elements [8l, 8l+8) of it), so a warp step covers two adjacent K blocks and
+// kU steps are unrolled to keep kU 16-byte loads per thread in flight.  All
+// lanes run every shuffle; loads and stores past the row's last K block are
+// skipped.  A CTA of 8 warps covers 8 consecutive rows, so the 8 scales of
+// one K block leave as one 32-byte segment.
+constexpr int kQ1Rows = 8;      // rows (warps) per CTA
+constexpr int kQ1U = 4;         // warp steps (tile pairs) unrolled per iteration
+
 template <bool POW2>
 __global__ void __launch_bounds__(256) quant_act_1x128_kernel(const uint16_t* __restrict__ x, int64_t M, int64_t K,
                                                               int64_t ldx, uint8_t* __restrict__ q,
                                                               float* __restrict__ s) {
-    constexpr int U = 2;                       // tile pairs in flight per warp
     const int lane = threadIdx.x & 31;
     const int half = lane >> 4;
     const int l16 = lane & 15;
-    const int64_t nkb = K >> 7;
-    const int64_t ntiles = M * nkb;
-    const int64_t npairs = (ntiles + 1) >> 1;
-    const int64_t warp = (int64_t(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
-    const int64_t nwarps = (int64_t(gridDim.x) * blockDim.x) >> 5;
+    const int64_t m = int64_t(blockIdx.x) * kQ1Rows + (threadIdx.x >> 5);
+    if (m >= M) return;                                   // warp-uniform
+    const int nkb = int(K >> 7);
+    const uint4* xr = reinterpret_cast<const uint4*>(x + m * ldx) + l16;   // + 16 * kb per tile
+    uint2* qr = reinterpret_cast<uint2*>(q + m * K) + l16;                  // + 16 * kb per tile
 
-    for (int64_t p0 = warp * U; p0 < npairs; p0 += nwarps * U) {
-        uint4 v[U];
-        int64_t tile[U];
+    for (int kb0 = 0; kb0 < nkb; kb0 += 2 * kQ1U) {
+        uint4 v[kQ1U];
 #pragma unroll
-        for (int u = 0; u < U; ++u) {
-            tile[u] = (p0 + u) * 2 + half;
-            v[u] = make_uint4(0, 0, 0, 0);
-            if (p0 + u < npairs && tile[u] < ntiles) {
-                const int64_t m = tile[u] / nkb, kb = tile[u] - m * nkb;
-                v[u] = __ldg(reinterpret_cast<const uint4*>(x + m * ldx + kb * 128) + l16);
-            }
+        for (int u = 0; u < kQ1U; ++u) {
+            const int kb = kb0 + 2 * u + half;
+            v[u] = kb < nkb ? __ldg(xr + 16 * kb) : make_uint4(0, 0, 0, 0);
         }
 #pragma unroll
-        for (int u = 0; u < U; ++u) {
+        for (int u = 0; u < kQ1U; ++u) {
+            const int kb = kb0 + 2 * u + half;
             const uint32_t w[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
             float f[8];
 #pragma unroll
@@ -77,15 +76,14 @@ __global__ void __launch_bounds__(256) quant_act_1x128_kernel(const uint16_t* __
             for (int o = 8; o >= 1; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, o));
             float inv;
             const float sc = tile_scale(amax, POW2, inv);
-            if (p0 + u < npairs && tile[u] < ntiles) {
-                const int64_t m = tile[u] / nkb, kb = tile[u] - m * nkb;
+            if (kb < nkb) {
                 uint2 o;
                 o.x = cvt_e4m3x2(__fmul_rn(f[0], inv), __fmul_rn(f[1], inv)) |
                       (cvt_e4m3x2(__fmul_rn(f[2], inv), __fmul_rn(f[3], inv)) << 16);
                 o.y = cvt_e4m3x2(__fmul_rn(f[4], inv), __fmul_rn(f[5], inv)) |
                       (cvt_e4m3x2(__fmul_rn(f[6], inv), __fmul_rn(f[7], inv)) << 16);
-                reinterpret_cast<uint2*>(q + m * K + kb * 128)[l16] = o;
-                if (l16 == 0) s[kb * M + m] = sc;
+                qr[16 * kb] = o;
+                if (l16 == 0) s[int64_t(kb) * M + m] = sc;
             }
         }
     }
@@ -259,11 +257,9 @@ extern "C" int fp8_quant_act_1x128(const uint16_t* x, int64_t M, int64_t K, int6
     if (!x || !q || !s || M <= 0 || K <= 0 || ldx < K || (flags & ~FP8_SCALE_POW2)) return FP8_ERR_ARG;
     if (K % 128) return FP8_ERR_SHAPE;
     if (!aligned16(x) || !aligned16(q) || (ldx % 8) || (reinterpret_cast<uintptr_t>(s) & 3u)) return FP8_ERR_ALIGN;
-    const int64_t pairs = (M * (K / 128) + 1) / 2;
-    const int64_t warps_needed = (pairs + 1) / 2;
-    const int64_t blocks = (warps_needed + 7) / 8;
-    const int64_t cap = int64_t(num_sms()) * 8;
-    const int grid = int(blocks < cap ? blocks : cap);
+    const int64_t blocks = (M + kQ1Rows - 1) / kQ1Rows;
+    if (blocks > 0x7FFFFFFFll) return FP8_ERR_SHAPE;
+    const unsigned grid = unsigned(blocks);
     if (flags & FP8_SCALE_POW2)
         quant_act_1x128_kernel<true><<<grid, 256, 0, stream>>>(x, M, K, ldx, q, s);
     else
