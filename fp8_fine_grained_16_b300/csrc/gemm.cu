@@ -1,4 +1,4 @@
-// gemm.cu -- block-scaled FP8 GEMMs on tcgen05 (dense and MoE grouped).
+// gemm.cu -- block-scaled FP8 GEMMs on tcgen05 (dense, Wgrad and MoE grouped).
 //
 // What is computed (pages 2 and 3: partial sums are accumulated by the tensor
 // cores over a K interval, then copied out, multiplied by the scaling
@@ -8,40 +8,41 @@
 //   P_kb    = A[:, 128kb : 128kb+128] * B[:, 128kb : 128kb+128]^T   (E4M3 MMA)
 //
 // The pages' Hopper scheme overlaps promotion with WGMMA by ping-ponging two
-// warpgroups.  Here the overlap comes from tensor memory instead.  One CTA
-// per SM computes 128 x 256 output tiles:
+// warpgroups.  Here the overlap comes from tensor memory: the MMAs of K block
+// kb+1 fill one TMEM accumulator while the CUDA cores promote P_kb out of the
+// other.
 //
-//   warp 0        TMA producer.  Per K block one pipeline stage receives the
-//                 A tile (128 x 128 B), the B tile (256 x 128 B), both with
-//                 the 128-byte swizzle, and the scales the promotion needs:
-//                 sA of the tile's 128 rows and sB of its columns.
-//   warp 1        allocates TMEM and issues, per K block, four tcgen05.mma
-//                 (K = 32 each) into one of two TMEM accumulators (256 fp32
-//                 columns each), then commits to the stage's "empty" barrier
-//                 and the accumulator's "full" barrier.
+// One persistent kernel serves every form.  A cluster of two CTAs on
+// neighbouring SMs computes 256 x 256 output tiles with
+// tcgen05.mma.cta_group::2 (M = 256): each CTA holds its 128 rows of A and
+// half of the B tile in its own shared memory, and each CTA's TMEM receives
+// its 128 rows of D.  Per K block a CTA moves 32 KB of operands through
+// shared memory for 128 x 256 x 128 multiply-adds (a one-CTA 128 x 256 tile
+// moves 48 KB for the same work).  Roles, per CTA:
+//
+//   warp 0        TMA producer: A and B halves (128-byte swizzle) and the
+//                 scales the promotion needs (sA of the CTA's 128 rows, sB of
+//                 the tile's columns) into a 6-stage ring.
+//   warp 1        allocates the pair's TMEM (two 256-column fp32
+//                 accumulators); in the leader CTA it issues four MMAs
+//                 (K = 32 each) per K block and commits them to both CTAs'
+//                 barriers.
 //   warps 2, 3    idle (they only give their registers to the promotion warps)
 //   warps 4..11   promotion: two warpgroups, one per 128-column half.  Thread
-//                 (warp w, lane l) owns tile row 32*(w%4)+l (TMEM lanes are
-//                 tied to w%4).  Per K block it reads P_kb from TMEM in two
-//                 64-column batches, frees the accumulator (one arrive per
-//                 warp) as soon as the second batch is in registers, and adds
-//                 P_kb * sA*sB into 128 fp32 registers with packed two-lane
-//                 FMAs.  Meanwhile the MMA warp already fills the other
-//                 accumulator with P_{kb+1}.  A stage is refilled only after
-//                 the MMAs and all eight promotion warps are done with it.
+//                 (warp w, lane l) owns row 32*(w%4)+l of its CTA's 128 rows
+//                 (TMEM lanes are tied to w%4).  Per K block it reads P_kb
+//                 from TMEM 32 columns at a time, frees the accumulator once
+//                 all of it is in registers, and adds P_kb * sA*sB into 128
+//                 fp32 registers with packed two-lane FMAs.
 //
-// An mbarrier probe costs a couple of hundred cycles on this part even when
-// the phase has completed, so each role tests the two barriers it needs per
-// K block in one combined probe.
-//
-// The kernel is persistent: one CTA per SM walks a static list of output
-// tiles; stage and accumulator indices run on across tile boundaries, so the
+// The kernel is persistent: each cluster walks a static list of pair tiles;
+// stage and accumulator indices run on across tile boundaries, so the
 // epilogue of one tile overlaps the first MMAs of the next.
 //
 // Every pipeline wait is bounded (2 s).  A wait that expires records
-// FP8_ERR_TIMEOUT in the device status word, raises a CTA-wide abort flag,
+// FP8_ERR_TIMEOUT in the device status word, raises the CTA's abort flag,
 // and lets the CTA drain its copies in flight, release its tensor memory and
-// exit.
+// exit (both CTAs meet at a final cluster barrier first).
 #include <cudaTypedefs.h>
 
 #include "common.cuh"
@@ -57,9 +58,6 @@ constexpr int BK = 128;                 // K block = promotion interval = scale 
 constexpr int kThreads = 384;           // 12 warps = 3 warpgroups
 constexpr int kPromoThreads = 256;      // warps 4..11
 constexpr int kPromoWarps = kPromoThreads / 32;
-// Register split: the block launches with 168 registers per thread (384 x 168
-// = 64512); warpgroup 0 (TMA, MMA, idle) gives back down to 40 and the two
-// promotion warpgroups grow to 232: 128*40 + 256*232 = 64512.
 constexpr int kTmemCols = 512;
 constexpr int kMaxExperts = 1024;
 // Scales travel in the pipeline stage through rank-1 TMA maps.  A tensor
@@ -72,27 +70,6 @@ constexpr int kSaRegion = 640;                   // bytes reserved for it in a s
 constexpr int kSbBox0 = 4;                       // BMODE 0: 16-byte box around one block scale
 constexpr int kSbHalf0 = 32;                     // BMODE 0: floats between the two halves' boxes (128 bytes)
 static_assert(kSaRegion % 128 == 0 && kSaRegion >= kSaBox * 4 && (kSbHalf0 * 4) % 128 == 0, "TMA box alignment");
-
-template <int BN, int STAGES, int BMODE, bool GROUPED>
-struct Layout {
-    static constexpr int kABytes = BM * BK;
-    static constexpr int kBBytes = BN * BK;
-    static constexpr int kSaOff = kABytes + kBBytes;                        // in a stage
-    static constexpr int kSbOff = kSaOff + kSaRegion;
-    static constexpr int kSbRegion = BMODE == 1 ? BN * 4 : 2 * kSbHalf0 * 4;
-    static constexpr int kStageBytes = (kSbOff + kSbRegion + 1023) & ~1023;
-    static constexpr uint32_t kTxBytes = kABytes + kBBytes + kSaBox * 4 + (BMODE == 1 ? BN * 4 : 2 * kSbBox0 * 4);
-    static constexpr int kStagesBytes = STAGES * kStageBytes;
-    static constexpr int kBarOff = kStagesBytes;  // full[S], empty[S], tfull[2], tempty[2], done
-    static constexpr int kNumBars = 2 * STAGES + 5;
-    static constexpr int kMiscOff = kBarOff + kNumBars * 8;       // tmem base, abort flag
-    static constexpr int kGrpOff = (kMiscOff + 16 + 15) & ~15;    // grouped: off[E+1], tile prefix[E+1]
-    static constexpr int kGrpBytes = GROUPED ? 2 * (kMaxExperts + 1) * 4 : 0;
-    static constexpr int kBytes = kGrpOff + kGrpBytes;
-    static constexpr int kDynSmem = kBytes + 1024;                // slack for 1024-byte alignment
-    static_assert(kABytes % 1024 == 0 && kStageBytes % 1024 == 0, "operand tiles start on 1024-byte boundaries");
-    static_assert(kSaOff % 128 == 0 && kSbOff % 128 == 0, "scale boxes start on 128-byte boundaries");
-};
 
 struct GemmArgs {
     const float* sa;
@@ -112,87 +89,136 @@ struct Tile {
     int32_t e;               // expert (grouped)
 };
 
-// ---------------------------------------------------------------- schedules
-// Dense: tile w -> m-tile w % num_m, n-tile w / num_m.  Consecutive tiles run
-// on neighbouring SMs at the same time and share their B panel in L2.
-struct DenseSched {
-    int64_t num_m, num_n, M;
-    FP8_DEV int64_t count() const { return num_m * num_n; }
+// ================================================================ kernel
+// The leader (rank 0) issues tcgen05.mma.cta_group::2; both CTAs keep their
+// A rows and B half at the same shared-memory offsets.
+//
+//   producer (warp 0, each CTA)  TMA-loads its A and B halves, counted on the
+//                                leader's full[s] (the leader expects both
+//                                CTAs' bytes), and its own scales, counted on
+//                                its own sfull[s].
+//   MMA (warp 1, leader only)    waits full[s], issues four MMAs, and commits
+//                                to empty[s] and sfull[s] of both CTAs
+//                                (multicast).
+//   promotion (warps 4..11)      on the CTA's own TMEM rows.
+//
+// Every role waits on one barrier per K block (a probe costs ~190 cycles):
+//   full[s]  (leader)  = producer's arrival + both CTAs' operand bytes + the
+//                        16 promotion warps that freed the TMEM accumulator
+//                        this K block will overwrite (K block g uses buffer
+//                        g % 2, freed by the promotion of K block g - 2; the
+//                        first two K blocks find their buffers free: every
+//                        promotion warp pre-arrives on full[0] and full[1]).
+//   sfull[s] (each)    = producer's arrival + this CTA's scale bytes + the
+//                        MMA commit of that K block (its accumulator is ready).
+//   empty[s] (each)    = MMA commit + this CTA's 8 promotion warps.
+constexpr int kPairStages = 6;
+// Register split (launched with 168 per thread, 64512 in all): warpgroup 0
+// keeps 64 (the producer's per-K-block state spills at 40), the promotion
+// warpgroups get 216 (128 accumulators + one 32-column TMEM batch +
+// addressing):
+// 128*64 + 256*216 = 63488 <= 64512.
+constexpr int kPairRegsWG0 = 64, kPairRegsPromo = 216;
+static_assert(128 * kPairRegsWG0 + 256 * kPairRegsPromo <= kThreads * 168, "register split");
+
+template <int BN, int STAGES, int BMODE, bool GROUPED>
+struct PairLayout {
+    static constexpr int kABytes = BM * BK;                      // this CTA's 128 rows
+    static constexpr int kBBytes = (BN / 2) * BK;                // this CTA's half of B
+    static constexpr int kSaOff = kABytes + kBBytes;
+    static constexpr int kSbOff = kSaOff + kSaRegion;
+    static constexpr int kSbRegion = BMODE == 1 ? BN * 4 : 2 * kSbHalf0 * 4;
+    static constexpr int kStageBytes = (kSbOff + kSbRegion + 1023) & ~1023;
+    static constexpr uint32_t kPairTxBytes = 2 * (kABytes + kBBytes);   // leader's full[s]: both CTAs
+    static constexpr uint32_t kScaleTxBytes = kSaBox * 4 + (BMODE == 1 ? BN * 4 : 2 * kSbBox0 * 4);
+    static constexpr int kStagesBytes = STAGES * kStageBytes;
+    static constexpr int kBarOff = kStagesBytes;  // full[S], sfull[S], empty[S], done
+    static constexpr int kNumBars = 3 * STAGES + 1;
+    static constexpr int kMiscOff = kBarOff + kNumBars * 8;       // tmem base, abort flag
+    static constexpr int kGrpOff = (kMiscOff + 16 + 15) & ~15;
+    static constexpr int kGrpBytes = GROUPED ? 2 * (kMaxExperts + 1) * 4 : 0;
+    static constexpr int kBytes = kGrpOff + kGrpBytes;
+    static constexpr int kDynSmem = kBytes + 1024;
+    static_assert(kABytes % 1024 == 0 && kBBytes % 1024 == 0 && kStageBytes % 1024 == 0,
+                  "operand tiles start on 1024-byte boundaries");
+    static_assert(kSaOff % 128 == 0 && kSbOff % 128 == 0, "scale boxes start on 128-byte boundaries");
+    static_assert(kDynSmem <= 232448, "shared memory per CTA");
+};
+
+// Dense pair tiles: w -> pair row tile w % num_m2 (256 rows), column tile w / num_m2.
+struct DensePairSched {
+    int64_t num_m2, num_n, M;
+    FP8_DEV int64_t count() const { return num_m2 * num_n; }
     FP8_DEV Tile get(int64_t w) const {
         Tile t;
-        const int64_t mt = w % num_m, nt = w / num_m;
-        t.row0 = mt * BM;
+        t.row0 = (w % num_m2) * (2 * BM);
         t.row_end = M;
-        t.n0 = int32_t(nt);   // column tile index; the kernel scales it by BN
+        t.n0 = int32_t(w / num_m2);
         t.e = 0;
         return t;
     }
 };
 
-// Grouped: expert e has mt_e = ceil(rows_e / 128) row tiles; the work list
-// holds, for each expert in order, its num_n column tiles x mt_e row tiles
-// with the row tile innermost, so that the row tiles of one (expert, column
-// tile) run side by side and read the weight tile from HBM once.
-struct GroupedSched {
-    const int32_t* off_s;    // smem, offsets [E+1]
-    const int32_t* pre_s;    // smem, prefix of row-tile counts [E+1]
+// Grouped pair tiles: expert e has ceil(ceil(rows_e / 128) / 2) row-tile
+// pairs; per expert, its column tiles x row pairs with the row pair innermost.
+struct GroupedPairSched {
+    const int32_t* off_s;
+    const int32_t* pre_s;    // prefix of row-pair counts [E+1]
     int E;
     int64_t num_n;
     FP8_DEV int64_t count() const { return int64_t(pre_s[E]) * num_n; }
     FP8_DEV Tile get(int64_t w) const {
-        int lo = 0, hi = E;                 // find e: pre[e]*num_n <= w < pre[e+1]*num_n
+        int lo = 0, hi = E;
         while (hi - lo > 1) {
             const int mid = (lo + hi) >> 1;
             if (int64_t(pre_s[mid]) * num_n <= w) lo = mid; else hi = mid;
         }
         const int e = lo;
-        const int64_t mt = pre_s[e + 1] - pre_s[e];
+        const int64_t mt2 = pre_s[e + 1] - pre_s[e];
         const int64_t local = w - int64_t(pre_s[e]) * num_n;
         Tile t;
         t.e = e;
-        t.n0 = int32_t(local / mt);        // column tile index; the kernel scales it by BN
-        t.row0 = int64_t(off_s[e]) + (local % mt) * BM;
+        t.n0 = int32_t(local / mt2);
+        t.row0 = int64_t(off_s[e]) + (local % mt2) * (2 * BM);
         t.row_end = off_s[e + 1];
         return t;
     }
 };
 
-// ---------------------------------------------------------------- kernel
 template <int BN, int STAGES, int BMODE, bool OUT_F32, bool GROUPED>
 __global__ void __launch_bounds__(kThreads, 1)
-    gemm_blockscaled_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                            const __grid_constant__ CUtensorMap tmSA, const __grid_constant__ CUtensorMap tmSB,
-                            const GemmArgs args) {
-    using L = Layout<BN, STAGES, BMODE, GROUPED>;
+    gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                     const __grid_constant__ CUtensorMap tmSA, const __grid_constant__ CUtensorMap tmSB,
+                     const GemmArgs args) {
+    using L = PairLayout<BN, STAGES, BMODE, GROUPED>;
     static_assert(2 * BN <= kTmemCols, "two accumulators must fit in TMEM");
     static_assert(BN == 256, "one promotion half = 128 columns = one scale block and one column per warpgroup thread");
-    constexpr int kHalf = BN / 2;          // columns per promotion warpgroup
-    constexpr uint32_t kIdesc = idesc_e4m3_f32(BM, BN);
+    constexpr int kHalf = BN / 2;
+    constexpr uint32_t kIdesc = idesc_e4m3_f32(2 * BM, BN);     // M = 256 across the pair
 
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::kBarOff);
-    uint64_t* full = bars;
-    uint64_t* empty = bars + STAGES;
-    uint64_t* tfull = bars + 2 * STAGES;
-    uint64_t* tempty = bars + 2 * STAGES + 2;
-    uint64_t* done = bars + 2 * STAGES + 4;
+    uint64_t* full = bars;                       // leader: operands of both CTAs + accumulator free
+    uint64_t* sfull = bars + STAGES;             // own scales + accumulator ready
+    uint64_t* empty = bars + 2 * STAGES;         // MMA commit + own promotion warps
+    uint64_t* done = bars + 3 * STAGES;
     uint32_t* tmem_base_s = reinterpret_cast<uint32_t*>(smem + L::kMiscOff);
     volatile int* abort_s = reinterpret_cast<volatile int*>(smem + L::kMiscOff + 4);
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
+    const uint32_t rank = cluster_ctarank();
+    const bool leader = rank == 0;
     const int64_t nkb = args.K / BK;
+    const int64_t cluster = blockIdx.x >> 1, nclusters = gridDim.x >> 1;
 
     // ---------------- set-up
     if (threadIdx.x == 0) {
         for (int i = 0; i < STAGES; ++i) {
-            mbar_init(&full[i], 1);
-            mbar_init(&empty[i], 1 + kPromoWarps);          // MMA commit + every promotion warp
-        }
-        for (int i = 0; i < 2; ++i) {
-            mbar_init(&tfull[i], 1);
-            mbar_init(&tempty[i], kPromoWarps);             // one arrive per promotion warp
+            mbar_init(&full[i], 1 + 2 * kPromoWarps);
+            mbar_init(&sfull[i], 2);
+            mbar_init(&empty[i], 1 + kPromoWarps);
         }
         mbar_init(done, 1);
         *abort_s = 0;
@@ -205,12 +231,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         tma_prefetch_desc(&tmSB);
     }
     if (warp == 1) {
-        tmem_alloc(tmem_base_s, kTmemCols);
-        tmem_relinquish();
+        tmem_alloc_pair(tmem_base_s, kTmemCols);
+        tmem_relinquish_pair();
     }
 
-    GroupedSched gs{};
-    DenseSched ds{};
+    GroupedPairSched gs{};
+    DensePairSched ds{};
     if constexpr (GROUPED) {
         int32_t* off_s = reinterpret_cast<int32_t*>(smem + L::kGrpOff);
         int32_t* pre_s = off_s + (kMaxExperts + 1);
@@ -219,7 +245,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int i = threadIdx.x; i <= E; i += kThreads) off_s[i] = __ldg(args.off + i);
         __syncthreads();
         if (warp == 0) {
-            // validate and build the prefix of row-tile counts, 32 experts per step
             int carry = 0;
             if (lane == 0) pre_s[0] = 0;
             for (int base = 0; base < E; base += 32) {
@@ -229,7 +254,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const int64_t lo = off_s[e], hi = off_s[e + 1];
                     const bool ok = lo >= 0 && lo <= hi && hi <= args.M;
                     bad |= !ok;
-                    cnt = ok ? int((hi - lo + BM - 1) / BM) : 0;
+                    cnt = ok ? int(((hi - lo + BM - 1) / BM + 1) / 2) : 0;
                 }
                 int incl = cnt;
 #pragma unroll
@@ -243,39 +268,40 @@ __global__ void __launch_bounds__(kThreads, 1)
             bad |= (lane == 0) && (off_s[0] != 0 || int64_t(off_s[E]) != args.M);
             if (__any_sync(0xFFFFFFFFu, bad) && lane == 0 && blockIdx.x == 0) record_status(FP8_ERR_OFFSETS);
         }
-        gs = GroupedSched{off_s, pre_s, E, (args.N + BN - 1) / BN};
+        gs = GroupedPairSched{off_s, pre_s, E, (args.N + BN - 1) / BN};
     } else {
-        ds = DenseSched{(args.M + BM - 1) / BM, (args.N + BN - 1) / BN, args.M};
+        ds = DensePairSched{(args.M + 2 * BM - 1) / (2 * BM), (args.N + BN - 1) / BN, args.M};
     }
     tc_fence_before();
-    __syncthreads();
+    // Both CTAs' barriers are initialised and the TMEM is allocated before
+    // either CTA touches the other's shared memory.
+    cluster_sync();
     tc_fence_after();
     const uint32_t tmem_base = *tmem_base_s;
 
-    // Both schedules return the column-tile index in n0; scale it to a column.
     auto tile_at = [&](int64_t w) -> Tile {
         Tile t;
         if constexpr (GROUPED) t = gs.get(w); else t = ds.get(w);
         t.n0 *= BN;
+        t.row0 += int64_t(rank) * BM;            // this CTA's 128 rows of the pair tile
         return t;
     };
     int64_t num_tiles;
     if constexpr (GROUPED) num_tiles = gs.count(); else num_tiles = ds.count();
-    // BMODE 0: index in sb of K block 0 of the 128x128 block scales of column
-    // half h of tile t (a half past N reads an in-bounds scale, never stored)
     auto sb_row = [&](const Tile& t, int h) -> int64_t {
         const int64_t c0 = int64_t(t.n0) + h * kHalf;
         return (int64_t(t.e) * (args.N / 128) + (c0 < args.N ? c0 : args.N - 1) / 128) * nkb;
     };
 
     if (warp < 4) {
-        asm volatile("setmaxnreg.dec.sync.aligned.u32 40;");
+        asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kPairRegsWG0));
         if (warp == 0) {
-            // ================= TMA producer
+            // ================= TMA producer (each CTA)
             if (lane == 0) {
+                const uint32_t full0 = mapa_shared(&full[0], 0);    // leader's full[0], cluster address
                 uint32_t it = 0;
                 bool ok = true;
-                for (int64_t w = blockIdx.x; ok && w < num_tiles; w += gridDim.x) {
+                for (int64_t w = cluster; ok && w < num_tiles; w += nclusters) {
                     const Tile t = tile_at(w);
                     int64_t sbr[2] = {0, 0};
                     if constexpr (BMODE == 0) {
@@ -289,47 +315,51 @@ __global__ void __launch_bounds__(kThreads, 1)
                             break;
                         }
                         uint8_t* st = smem + stage * L::kStageBytes;
-                        mbar_arrive_expect_tx(&full[stage], L::kTxBytes);
-                        tma_load_2d(st, &tmA, &full[stage], int32_t(kb * BK), int32_t(t.row0));
+                        const uint32_t fbar = full0 + stage * 8;
+                        if (leader) mbar_arrive_expect_tx(&full[stage], L::kPairTxBytes);
+                        tma_load_2d_pair(st, &tmA, fbar, int32_t(kb * BK), int32_t(t.row0));
                         if constexpr (GROUPED)
-                            tma_load_3d(st + L::kABytes, &tmB, &full[stage], int32_t(kb * BK), t.n0, t.e);
+                            tma_load_3d_pair(st + L::kABytes, &tmB, fbar, int32_t(kb * BK),
+                                             t.n0 + int32_t(rank) * (BN / 2), t.e);
                         else
-                            tma_load_2d(st + L::kABytes, &tmB, &full[stage], int32_t(kb * BK), t.n0);
-                        tma_load_1d(st + L::kSaOff, &tmSA, &full[stage], int32_t((kb * args.M + t.row0) & ~int64_t(3)));
+                            tma_load_2d_pair(st + L::kABytes, &tmB, fbar, int32_t(kb * BK),
+                                             t.n0 + int32_t(rank) * (BN / 2));
+                        mbar_arrive_expect_tx(&sfull[stage], L::kScaleTxBytes);
+                        tma_load_1d(st + L::kSaOff, &tmSA, &sfull[stage], int32_t((kb * args.M + t.row0) & ~int64_t(3)));
                         if constexpr (BMODE == 0) {
-                            tma_load_1d(st + L::kSbOff, &tmSB, &full[stage], int32_t((sbr[0] + kb) & ~int64_t(3)));
-                            tma_load_1d(st + L::kSbOff + kSbHalf0 * 4, &tmSB, &full[stage],
+                            tma_load_1d(st + L::kSbOff, &tmSB, &sfull[stage], int32_t((sbr[0] + kb) & ~int64_t(3)));
+                            tma_load_1d(st + L::kSbOff + kSbHalf0 * 4, &tmSB, &sfull[stage],
                                         int32_t((sbr[1] + kb) & ~int64_t(3)));
                         } else {
-                            tma_load_1d(st + L::kSbOff, &tmSB, &full[stage], int32_t(kb * args.N + t.n0));
+                            tma_load_1d(st + L::kSbOff, &tmSB, &sfull[stage], int32_t(kb * args.N + t.n0));
                         }
                         ++it;
                     }
                 }
                 if (!ok) record_status(FP8_ERR_TIMEOUT);
-                // Let every copy this thread issued land before the CTA can exit.
-                // Only this thread arrives on full[], so the latest phase of each
-                // stage is the one of its last issued load.
+                // Let this CTA's copies land before it can leave: its scales on
+                // its own sfull[]; both CTAs' operand tiles on the leader's full[]
+                // (the final cluster barrier holds the other CTA until then).
                 int zero = 0;
                 const uint32_t first = it > STAGES ? it - STAGES : 0;
-                for (uint32_t j = first; j < it; ++j)
-                    mbar_wait_bounded(&full[j % STAGES], (j / STAGES) & 1u, reinterpret_cast<volatile int*>(&zero));
+                for (uint32_t j = first; j < it; ++j) {
+                    mbar_wait_bounded(&sfull[j % STAGES], (j / STAGES) & 1u, reinterpret_cast<volatile int*>(&zero));
+                    if (leader)
+                        mbar_wait_bounded(&full[j % STAGES], (j / STAGES) & 1u, reinterpret_cast<volatile int*>(&zero));
+                }
             }
             __syncwarp();
         } else if (warp == 1) {
-            // ================= MMA issuer
-            if (lane == 0) {
+            // ================= MMA issuer (leader only)
+            if (leader && lane == 0) {
                 uint32_t it = 0, g = 0;
                 bool ok = true;
-                for (int64_t w = blockIdx.x; ok && w < num_tiles; w += gridDim.x) {
+                for (int64_t w = cluster; ok && w < num_tiles; w += nclusters) {
                     for (int64_t kb = 0; kb < nkb; ++kb) {
-                        const uint32_t buf = g & 1u, tphase = (g >> 1) & 1u;
+                        const uint32_t buf = g & 1u;
                         const uint32_t stage = it % STAGES, phase = (it / STAGES) & 1u;
-                        // the stage is usually loaded long before the accumulator frees up
-                        if (!mbar_test_wait2(&full[stage], phase, &tempty[buf], tphase ^ 1u)) {
-                            if (!mbar_wait_bounded(&full[stage], phase, abort_s)) { ok = false; break; }
-                            if (!mbar_wait_bounded(&tempty[buf], tphase ^ 1u, abort_s)) { ok = false; break; }
-                        }
+                        // operands of both CTAs landed and accumulator `buf` is free
+                        if (!mbar_wait_bounded(&full[stage], phase, abort_s)) { ok = false; break; }
                         tc_fence_after();
                         const uint32_t a_addr = smem_u32(smem + stage * L::kStageBytes);
                         const uint32_t b_addr = a_addr + L::kABytes;
@@ -337,75 +367,74 @@ __global__ void __launch_bounds__(kThreads, 1)
                         const uint64_t bdesc = sw128_kmajor_desc(b_addr);
                         const uint32_t d_tmem = tmem_base + buf * BN;
 #pragma unroll
-                        for (int k = 0; k < BK / 32; ++k)      // K = 32 bytes per MMA: +2 in the >>4 address field
-                            umma_e4m3(d_tmem, adesc + 2 * k, bdesc + 2 * k, kIdesc, k > 0 ? 1u : 0u);
-                        umma_commit(&empty[stage]);
-                        umma_commit(&tfull[buf]);
+                        for (int k = 0; k < BK / 32; ++k)
+                            umma_e4m3_pair(d_tmem, adesc + 2 * k, bdesc + 2 * k, kIdesc, k > 0 ? 1u : 0u);
+                        umma_commit_pair(&empty[stage], 0x3);
+                        umma_commit_pair(&sfull[stage], 0x3);      // accumulator ready, in both CTAs
                         ++it;
                         ++g;
                     }
                 }
                 if (!ok) record_status(FP8_ERR_TIMEOUT);
-                // all MMAs issued by this thread are complete once `done` flips
-                umma_commit(done);
+                umma_commit_pair(done, 0x1);
                 int zero = 0;
                 mbar_wait_bounded(done, 0, reinterpret_cast<volatile int*>(&zero));
             }
             __syncwarp();
         }
     } else {
-        asm volatile("setmaxnreg.inc.sync.aligned.u32 232;");
-        // ================= promotion warpgroups
-        const int wq = warp & 3;                       // TMEM lane quarter of this warp
-        const int half = (warp - 4) >> 2;              // 0: columns [0, BN/2), 1: [BN/2, BN)
-        const int r = wq * 32 + lane;                  // tile row
+        asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kPairRegsPromo));
+        // ================= promotion warpgroups (each CTA, its own 128 rows)
+        const int wq = warp & 3;
+        const int half = (warp - 4) >> 2;
+        const int r = wq * 32 + lane;
         const uint32_t t_lane = uint32_t(wq * 32) << 16;
+        const uint32_t full0 = mapa_shared(&full[0], 0);       // leader's full[0], cluster address
+        // the two accumulators start out free: release them to K blocks 0 and 1
+        __syncwarp();
+        if (lane == 0) {
+            mbar_arrive_cluster(full0);
+            mbar_arrive_cluster(full0 + 8);
+        }
 
         uint32_t g = 0;
         bool ok = true;
-        for (int64_t w = blockIdx.x; ok && w < num_tiles; w += gridDim.x) {
+        for (int64_t w = cluster; ok && w < num_tiles; w += nclusters) {
             const Tile t = tile_at(w);
-            const int64_t m = t.row0 + r;
-            const int64_t ncol0 = int64_t(t.n0) + half * kHalf;   // first column of this thread's half
-            // N % 128 == 0, so a half tile (128 columns) is either entirely
-            // inside [0, N) or entirely past it (last tile of an N that is an
-            // odd multiple of 128).
-            const bool cols_ok = ncol0 < args.N;
-            const int64_t sbr = BMODE == 0 ? sb_row(t, half) : 0;
+            // Where this K block's scales sit in the stage's boxes: the sA box
+            // starts at (kb*M + row0) rounded down to 4 elements, the BMODE-0 sB
+            // box at (sb_row + kb) rounded down to 4.  Both offsets advance by a
+            // constant per K block (mod 4).
+            const int sa_off0 = int(t.row0 & 3), m_step = int(args.M & 3);
+            const int sb_off0 = BMODE == 0 ? int(sb_row(t, half) & 3) : 0;
 
             float2 acc[kHalf / 2];
 #pragma unroll
             for (int i = 0; i < kHalf / 2; ++i) acc[i] = make_float2(0.0f, 0.0f);
 
-            for (int64_t kb = 0; kb < nkb; ++kb) {
+            for (int kb = 0; kb < int(nkb); ++kb) {
                 const uint32_t stage = g % STAGES, phase = (g / STAGES) & 1u;
-                const uint32_t buf = g & 1u, tphase = (g >> 1) & 1u;
-                // Lane 0 waits for this K block's stage (its scales) and
-                // accumulator; __syncwarp passes the acquire on to the other
-                // lanes, and the warp leaves the loop as a whole if a wait
-                // gave up (the tcgen05 loads below are warp-collective).
+                const uint32_t buf = g & 1u;
+                // scales landed and the MMAs of this K block are done
                 bool got = true;
-                if (lane == 0 && !mbar_test_wait2(&full[stage], phase, &tfull[buf], tphase))
-                    got = mbar_wait_bounded(&full[stage], phase, abort_s) &&
-                          mbar_wait_bounded(&tfull[buf], tphase, abort_s);
+                if (lane == 0) got = mbar_wait_bounded(&sfull[stage], phase, abort_s);
                 got = __shfl_sync(0xFFFFFFFFu, got ? 1 : 0, 0) != 0;
                 __syncwarp();
                 if (!got) { ok = false; break; }
                 tc_fence_after();
 
                 const uint8_t* st = smem + stage * L::kStageBytes;
-                // the sA box starts at (kb*M + row0) rounded down to 4 elements
-                const float sa_cur = reinterpret_cast<const float*>(st + L::kSaOff)[int((kb * args.M + t.row0) & 3) + r];
+                const float sa_cur = reinterpret_cast<const float*>(st + L::kSaOff)[((sa_off0 + kb * m_step) & 3) + r];
                 const float2 sa2 = make_float2(sa_cur, sa_cur);
                 float2 sc2 = sa2;
-                const float* sbk = reinterpret_cast<const float*>(st + L::kSbOff) + half * kHalf;   // BMODE 1
+                const float* sbk = reinterpret_cast<const float*>(st + L::kSbOff) + half * kHalf;
                 if constexpr (BMODE == 0) {
                     const float sbv =
-                        reinterpret_cast<const float*>(st + L::kSbOff)[half * kSbHalf0 + int((sbr + kb) & 3)];
+                        reinterpret_cast<const float*>(st + L::kSbOff)[half * kSbHalf0 + ((sb_off0 + kb) & 3)];
                     const float sc = __fmul_rn(sa_cur, sbv);
                     sc2 = make_float2(sc, sc);
                     __syncwarp();
-                    if (lane == 0) mbar_arrive(&empty[stage]);      // this warp is done with the stage
+                    if (lane == 0) mbar_arrive(&empty[stage]);
                 }
 
                 auto scale_chunk = [&](int c, const uint32_t (&v)[32]) {
@@ -432,36 +461,35 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                 };
 
+                // 32 columns at a time: a TMEM load round trip is short, and one
+                // 32-register batch leaves the accumulators room
                 const uint32_t tcol = tmem_base + t_lane + buf * BN + half * kHalf;
-                uint32_t va[32], vb[32];
-                // columns [0, 64) of this half
-                tmem_ld_32x32b_x32(tcol, va);
-                tmem_ld_32x32b_x32(tcol + 32, vb);
-                tmem_wait_ld_regs(va);
-                regs_fence(vb);
-                scale_chunk(0, va);
-                scale_chunk(1, vb);
-                // columns [64, 128); once they are in registers the accumulator
-                // is free for the MMAs two K blocks ahead
-                tmem_ld_32x32b_x32(tcol + 64, va);
-                tmem_ld_32x32b_x32(tcol + 96, vb);
-                tmem_wait_ld_regs(va);
-                regs_fence(vb);
+                uint32_t v[32];
+#pragma unroll
+                for (int c = 0; c < 3; ++c) {
+                    tmem_ld_32x32b_x32(tcol + 32 * c, v);
+                    tmem_wait_ld_regs(v);
+                    scale_chunk(c, v);
+                }
+                tmem_ld_32x32b_x32(tcol + 96, v);
+                tmem_wait_ld_regs(v);
                 tc_fence_before();
                 __syncwarp();
-                if (lane == 0) mbar_arrive(&tempty[buf]);
-                scale_chunk(2, va);
-                scale_chunk(3, vb);
+                // all of P_kb is in registers: accumulator `buf` is free for K
+                // block g + 2 (on the leader's full[])
+                if (lane == 0) mbar_arrive_cluster(full0 + ((g + 2) % STAGES) * 8);
+                scale_chunk(3, v);
                 if constexpr (BMODE == 1) {
                     __syncwarp();
-                    if (lane == 0) mbar_arrive(&empty[stage]);      // column scales no longer read
+                    if (lane == 0) mbar_arrive(&empty[stage]);
                 }
                 ++g;
             }
             if (!ok) break;
 
-            // ---- epilogue: this thread's row, BN/2 consecutive columns
-            if (cols_ok && m < t.row_end && m < args.M) {
+            const int64_t m = t.row0 + r;
+            const int64_t ncol0 = int64_t(t.n0) + half * kHalf;
+            if (ncol0 < args.N && m < t.row_end && m < args.M) {
                 if constexpr (OUT_F32) {
                     float* dst = reinterpret_cast<float*>(args.d) + m * args.N + ncol0;
 #pragma unroll
@@ -483,12 +511,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!ok) record_status(FP8_ERR_TIMEOUT);
     }
 
-    // ---------------- tear-down
+    // ---------------- tear-down: neither CTA leaves (or frees TMEM) while the
+    // other may still use its shared memory or tensor memory
     tc_fence_before();
     __syncthreads();
+    cluster_sync();
     if (warp == 1) {
         tc_fence_after();
-        tmem_dealloc(tmem_base, kTmemCols);
+        tmem_dealloc_pair(tmem_base, kTmemCols);
     }
 }
 
@@ -547,23 +577,39 @@ static int device_sms() {
     return n;
 }
 
+constexpr int kBN = 256;
+
 template <int BN, int STAGES, int BMODE, bool OUT_F32, bool GROUPED>
-static int launch(const CUtensorMap& ma, const CUtensorMap& mb, const CUtensorMap& msa, const CUtensorMap& msb,
-                  const GemmArgs& args, int grid, cudaStream_t stream) {
-    using L = Layout<BN, STAGES, BMODE, GROUPED>;
-    auto kern = gemm_blockscaled_kernel<BN, STAGES, BMODE, OUT_F32, GROUPED>;
+static int launch_pair(const CUtensorMap& ma, const CUtensorMap& mb, const CUtensorMap& msa, const CUtensorMap& msb,
+                       const GemmArgs& args, int sms, cudaStream_t stream) {
+    using L = PairLayout<BN, STAGES, BMODE, GROUPED>;
+    auto kern = gemm_pair_kernel<BN, STAGES, BMODE, OUT_F32, GROUPED>;
     static bool attr_set = false;
     if (!attr_set) {
         if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kDynSmem) != cudaSuccess)
             return FP8_ERR_CUDA;
         attr_set = true;
     }
-    kern<<<grid, kThreads, L::kDynSmem, stream>>>(ma, mb, msa, msb, args);
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = L::kDynSmem;
+    cfg.stream = stream;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    int max_clusters = 0;
+    cfg.gridDim = dim3(2 * (sms / 2));
+    if (cudaOccupancyMaxActiveClusters(&max_clusters, kern, &cfg) != cudaSuccess || max_clusters <= 0)
+        return FP8_ERR_CUDA;
+    const int clusters = max_clusters < sms / 2 ? max_clusters : sms / 2;
+    cfg.gridDim = dim3(2 * clusters);
+    if (cudaLaunchKernelEx(&cfg, kern, ma, mb, msa, msb, args) != cudaSuccess) return FP8_ERR_CUDA;
     return cudaGetLastError() == cudaSuccess ? FP8_OK : FP8_ERR_CUDA;
 }
-
-constexpr int kBN = 256;
-constexpr int kStages = 4;
 
 // Self-test of the bounded wait: one thread waits on an mbarrier that nothing
 // will ever arrive on, gives up after timeout_ns and records FP8_ERR_TIMEOUT,
@@ -599,20 +645,20 @@ extern "C" int fp8_gemm_blockscaled(const uint8_t* a, const float* sa, const uin
     if (sms <= 0) return FP8_ERR_DEVICE;
     CUtensorMap ma, mb, msa, msb;
     const int64_t nsb = b_scale_mode == FP8_BSCALE_ROW ? N * (K / 128) : (N / 128) * (K / 128);
-    if (!make_operand_map(&ma, a, M, K, BM, 1, false) || !make_operand_map(&mb, b, N, K, kBN, 1, false) ||
+    if (!make_operand_map(&ma, a, M, K, BM, 1, false) || !make_operand_map(&mb, b, N, K, kBN / 2, 1, false) ||
         !make_scale_map(&msa, sa, M * (K / 128), kSaBox) ||
         !make_scale_map(&msb, sb, nsb, b_scale_mode == FP8_BSCALE_ROW ? kBN : kSbBox0))
         return FP8_ERR_CUDA;
     GemmArgs args{sa, sb, d, nullptr, M, N, K, 0};
-    const int64_t tiles = ((M + BM - 1) / BM) * ((N + kBN - 1) / kBN);
-    const int grid = int(tiles < sms ? tiles : sms);
+    const int64_t pair_tiles = ((M + 2 * BM - 1) / (2 * BM)) * ((N + kBN - 1) / kBN);
+    const int grid_sms = int(2 * pair_tiles < sms ? 2 * pair_tiles : sms);
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     if (b_scale_mode == FP8_BSCALE_BLOCK128) {
-        if (d_dtype == FP8_OUT_BF16) return launch<kBN, kStages, 0, false, false>(ma, mb, msa, msb, args, grid, s);
-        return launch<kBN, kStages, 0, true, false>(ma, mb, msa, msb, args, grid, s);
+        if (d_dtype == FP8_OUT_BF16) return launch_pair<kBN, kPairStages, 0, false, false>(ma, mb, msa, msb, args, grid_sms, s);
+        return launch_pair<kBN, kPairStages, 0, true, false>(ma, mb, msa, msb, args, grid_sms, s);
     }
-    if (d_dtype == FP8_OUT_BF16) return launch<kBN, kStages, 1, false, false>(ma, mb, msa, msb, args, grid, s);
-    return launch<kBN, kStages, 1, true, false>(ma, mb, msa, msb, args, grid, s);
+    if (d_dtype == FP8_OUT_BF16) return launch_pair<kBN, kPairStages, 1, false, false>(ma, mb, msa, msb, args, grid_sms, s);
+    return launch_pair<kBN, kPairStages, 1, true, false>(ma, mb, msa, msb, args, grid_sms, s);
 }
 
 extern "C" int fp8_grouped_gemm_blockscaled(const uint8_t* a, const float* sa, const uint8_t* b, const float* sb,
@@ -633,12 +679,12 @@ extern "C" int fp8_grouped_gemm_blockscaled(const uint8_t* a, const float* sa, c
     const int sms = device_sms();
     if (sms <= 0) return FP8_ERR_DEVICE;
     CUtensorMap ma, mb, msa, msb;
-    if (!make_operand_map(&ma, a, total_rows, K, BM, 1, false) || !make_operand_map(&mb, b, N, K, kBN, E, true) ||
+    if (!make_operand_map(&ma, a, total_rows, K, BM, 1, false) || !make_operand_map(&mb, b, N, K, kBN / 2, E, true) ||
         !make_scale_map(&msa, sa, total_rows * (K / 128), kSaBox) ||
         !make_scale_map(&msb, sb, int64_t(E) * (N / 128) * (K / 128), kSbBox0))
         return FP8_ERR_CUDA;
     GemmArgs args{sa, sb, d, expert_offsets, total_rows, N, K, E};
-    return launch<kBN, kStages, 0, false, true>(ma, mb, msa, msb, args, sms, reinterpret_cast<cudaStream_t>(stream));
+    return launch_pair<kBN, kPairStages, 0, false, true>(ma, mb, msa, msb, args, sms, reinterpret_cast<cudaStream_t>(stream));
 }
 
 extern "C" int fp8_selftest_wait_timeout(uint64_t timeout_ns, fp8_stream_t stream) {
