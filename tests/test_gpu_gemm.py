@@ -121,3 +121,32 @@ def test_wait_timeout_selftest_reports_status(fb):
     q, s = fb.fp8_quant_act_1x128(x)                   # the context is still usable
     torch.cuda.synchronize()
     assert int(q[0, 0]) == 0x7E
+
+
+@pytest.mark.parametrize("mode,out_dtype,K", [(0, torch.float32, 2048), (0, torch.bfloat16, 2048),
+                                              (1, torch.float32, 2048), (1, torch.float32, 8192)])
+def test_gemm_many_tiles_per_cluster_full_rows(fb, orc, mode, out_dtype, K):
+    """Every output column of every 7th row, on a problem where each CTA pair
+    walks several tiles and the pipeline rings wrap many times, run three times:
+    a race between the MMA, the TMA refills and the promotion shows up here as
+    scattered wrong elements that a few sampled columns can miss."""
+    M, N = 2048, 4096
+    a, b = rand_codes((M, K), 11), rand_codes((N, K), 12)
+    sa = rand_scales((K // 128, M), 13)
+    sb = rand_scales((N // 128, K // 128) if mode == 0 else (K // 128, N), 14)
+    rows = np.arange(0, M, 7)
+    ref = orc.gemm_blockscaled(a, sa, b, sb, mode, rows=rows, cols=np.arange(N))
+    A, SA, B, SB = _dev(a), _dev(sa), _dev(b), _dev(sb)
+    refmax = np.abs(ref).max()
+    for rep in range(3):
+        d = fb.fp8_gemm_blockscaled(A, SA, B, SB, mode, out_dtype)
+        got = to_np(d)[rows]
+        assert_gemm_close(got, ref, out_dtype == torch.bfloat16, orc, "many tiles mode%d K%d rep%d" % (mode, K, rep))
+        # Element-wise, far tighter than the tolerance above: the fp32 sum of
+        # at most 64 promoted K blocks is off by ~1e-6 of max|ref|, and a
+        # bf16 output by one bf16 rounding on top.  A corrupted element (a
+        # K block read from the wrong accumulator or stage) is off by far more.
+        err = np.abs(got - ref)
+        bound = 1e-5 * refmax + (np.abs(ref) * 2.0 ** -8 if out_dtype == torch.bfloat16 else 0.0)
+        n_bad = int((err > bound).sum())
+        assert n_bad == 0, "many tiles mode%d K%d rep%d: %d elements beyond the element-wise bound" % (mode, K, rep, n_bad)
