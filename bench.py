@@ -364,7 +364,15 @@ def measure_rows(F, S, dev, flush, pk):
     hbm_row("a3_quant_weight_128x128", ms, N * K * 3 + (N // 128) * (K // 128) * 4, "W [7168,7168]")
     ms = _time(lambda: F.fp8_gemm_blockscaled(qx, sx, qw, sw, 0, torch.bfloat16, d=y), reps, warm, flush, st)
     tensor_row("a4_gemm_dense", ms, GEMM_FLOP, "4096x7168x7168 -> bf16")
-    del x, w, qx, qw, y
+    # Dgrad: dX = dY W from the transposed 128x128-block codes of W
+    qwT, swT = F.fp8_transpose_128x128(qw, sw)
+    ms = _time(lambda: F.fp8_transpose_128x128(qw, sw, qwT, swT), reps, warm, flush, st)
+    hbm_row("a8_transpose_128x128", ms, 2 * N * K + 2 * (N // 128) * (K // 128) * 4, "W codes [7168,7168] -> W^T codes")
+    dy = (torch.randn((M, N), generator=torch.Generator(device=dev).manual_seed(3), device=dev) * 1e-3).to(torch.bfloat16)
+    qdy, sdy = F.fp8_quant_act_1x128(dy)
+    ms = _time(lambda: F.fp8_gemm_blockscaled(qdy, sdy, qwT, swT, 0, torch.bfloat16, d=y), reps, warm, flush, st)
+    tensor_row("a8_gemm_dgrad", ms, GEMM_FLOP, "dX = dY W, 4096x7168x7168 -> bf16")
+    del x, w, qx, qw, y, qwT, dy, qdy
 
     # Wgrad rows
     d = S.wgrad()

@@ -1,0 +1,92 @@
+// transpose.cu -- transposed copy of a 128x128-block-quantised E4M3 matrix,
+// for FP8 Dgrad (page 1: E4M3 on all tensors, Fprop, Dgrad and Wgrad; page 4:
+// weights are quantised per 128x128 block).
+//
+// The amax of a 128x128 block does not change when the block is transposed,
+// so quantising W^T per 128x128 block gives exactly the transposed codes and
+// the transposed grid of block scales of quantising W.  Dgrad,
+// dX = dY * W, is then the block-scaled GEMM with A = dY (1x128 tiles) and
+// B = W^T from this copy.
+//
+// One CTA (256 threads) per 128x128 byte tile.  Thread (warp w, lane l)
+// loads the 32-bit words at byte column 4l of the input rows 4q .. 4q+3
+// (q = w + 8j, j < 4): every load instruction of a warp reads whole 128-byte
+// rows.  Each 4x4 byte block is transposed in registers (byte permutes) and
+// lands in a shared tile whose word index is rotated by the writing lane, so
+// neither the stores nor the loads of shared memory conflict; the output
+// leaves as 16-byte pieces of whole 128-byte rows.
+#include "common.cuh"
+
+namespace fp8bs {
+
+// 4x4 byte transpose: in[r] holds bytes (r,0..3) little-endian; out[c] gets
+// bytes (0..3,c).
+FP8_DEV void transpose4x4(const uint32_t (&in)[4], uint32_t (&out)[4]) {
+    const uint32_t t0 = __byte_perm(in[0], in[1], 0x5140);   // a0 b0 a1 b1
+    const uint32_t t1 = __byte_perm(in[2], in[3], 0x5140);   // c0 d0 c1 d1
+    const uint32_t t2 = __byte_perm(in[0], in[1], 0x7362);   // a2 b2 a3 b3
+    const uint32_t t3 = __byte_perm(in[2], in[3], 0x7362);   // c2 d2 c3 d3
+    out[0] = __byte_perm(t0, t1, 0x5410);                    // a0 b0 c0 d0
+    out[1] = __byte_perm(t0, t1, 0x7632);                    // a1 b1 c1 d1
+    out[2] = __byte_perm(t2, t3, 0x5410);                    // a2 b2 c2 d2
+    out[3] = __byte_perm(t2, t3, 0x7632);                    // a3 b3 c3 d3
+}
+
+__global__ void __launch_bounds__(256) transpose_128x128_kernel(const uint8_t* __restrict__ q,
+                                                                const float* __restrict__ s, int64_t N,
+                                                                int64_t K, uint8_t* __restrict__ qT,
+                                                                float* __restrict__ sT) {
+    // T[c][slot]: output row c (= input column), 32 words = input rows 4*word ..
+    // 4*word+3; word `wd` of row c sits at slot (wd + c/4) % 32.
+    __shared__ uint32_t T[128 * 32];
+    const int64_t nkb = K >> 7, nnb = N >> 7;
+    const int64_t nb = blockIdx.x / nkb, kb = blockIdx.x - nb * nkb;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const uint8_t* src = q + (nb * 128) * K + kb * 128;
+
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        const int qd = warp + 8 * j;                       // input row quad: rows 4qd .. 4qd+3
+        uint32_t in[4], out[4];
+#pragma unroll
+        for (int r = 0; r < 4; ++r)
+            in[r] = __ldg(reinterpret_cast<const uint32_t*>(src + (4 * qd + r) * K) + lane);
+        transpose4x4(in, out);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const int c = 4 * lane + i;                    // input column = output row
+            T[c * 32 + ((qd + lane) & 31)] = out[i];
+        }
+    }
+    __syncthreads();
+    // output row c = t / 2, words 16h .. 16h+15 (h = t % 2), four 16-byte stores
+    const int c = threadIdx.x >> 1, h = threadIdx.x & 1;
+    uint8_t* dst = qT + (kb * 128 + c) * N + nb * 128 + 64 * h;
+#pragma unroll
+    for (int v = 0; v < 4; ++v) {
+        uint32_t w[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            const int wd = 16 * h + 4 * v + e;
+            w[e] = T[c * 32 + ((wd + (c >> 2)) & 31)];
+        }
+        reinterpret_cast<uint4*>(dst)[v] = make_uint4(w[0], w[1], w[2], w[3]);
+    }
+    if (threadIdx.x == 0) sT[kb * nnb + nb] = s[nb * nkb + kb];
+}
+
+}  // namespace fp8bs
+
+using namespace fp8bs;
+
+extern "C" int fp8_transpose_128x128(const uint8_t* q, const float* s, int64_t N, int64_t K, uint8_t* qT, float* sT,
+                                     fp8_stream_t stream) {
+    if (!q || !s || !qT || !sT || N <= 0 || K <= 0) return FP8_ERR_ARG;
+    if (N % 128 || K % 128) return FP8_ERR_SHAPE;
+    if (!aligned16(q) || !aligned16(qT) || ((reinterpret_cast<uintptr_t>(s) | reinterpret_cast<uintptr_t>(sT)) & 3u))
+        return FP8_ERR_ALIGN;
+    const int64_t blocks = (N / 128) * (K / 128);
+    if (blocks > 0x7FFFFFFFll) return FP8_ERR_SHAPE;
+    transpose_128x128_kernel<<<unsigned(blocks), 256, 0, reinterpret_cast<cudaStream_t>(stream)>>>(q, s, N, K, qT, sT);
+    return cudaGetLastError() == cudaSuccess ? FP8_OK : FP8_ERR_CUDA;
+}

@@ -46,6 +46,7 @@ _SIGS = {
     "fp8_quant_act_128x1": [_P, _I64, _I64, _I64, _P, _P, _U32, _P],
     "fp8_quant_weight_128x128": [_P, _I64, _I64, _I64, _P, _P, _U32, _P],
     "fp8_gemm_blockscaled": [_P, _P, _P, _P, _I, _P, _I, _I64, _I64, _I64, _P],
+    "fp8_transpose_128x128": [_P, _P, _I64, _I64, _P, _P, _P],
     "fp8_grouped_gemm_blockscaled": [_P, _P, _P, _P, _P, _I, _I64, _I64, _I64, _P, _P],
     "fp8_moe_route_topk": [_P, _I64, _I, _I, _P, _P, _P, _P, _P, _P, _P],
     "fp8_moe_route_topk_noalloc": [_P, _I64, _I, _I, _P, _P, _P, _P, _P, _P],
@@ -171,6 +172,18 @@ def fp8_gemm_blockscaled(a, sa, b, sb, b_scale_mode: int = FP8_BSCALE_BLOCK128, 
         _ptr(a, torch.uint8, "a"), _ptr(sa, torch.float32, "sa"), _ptr(b, torch.uint8, "b"),
         _ptr(sb, torch.float32, "sb"), b_scale_mode, _ptr(d, None, "d"), d_dtype, M, N, K, _stream(stream)))
     return d
+
+
+def fp8_transpose_128x128(q, s, qT=None, sT=None, stream=None):
+    """q u8 [N, K], s f32 [N/128, K/128] -> (qT u8 [K, N], sT f32 [K/128, N/128]):
+    the 128x128-block quantisation of the transposed matrix (for Dgrad)."""
+    N, K = q.shape
+    qT = torch.empty((K, N), dtype=torch.uint8, device=q.device) if qT is None else qT
+    sT = torch.empty((K // 128, N // 128), dtype=torch.float32, device=q.device) if sT is None else sT
+    _check("fp8_transpose_128x128", lib.fp8_transpose_128x128(
+        _ptr(q, torch.uint8, "q"), _ptr(s, torch.float32, "s"), N, K, _ptr(qT, torch.uint8, "qT"),
+        _ptr(sT, torch.float32, "sT"), _stream(stream)))
+    return qT, sT
 
 
 def fp8_grouped_gemm_blockscaled(a, sa, b, sb, expert_offsets, d=None, stream=None) -> torch.Tensor:

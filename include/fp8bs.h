@@ -150,6 +150,21 @@ FP8_API int fp8_gemm_blockscaled(const uint8_t* a, const float* sa,
                                  fp8_stream_t stream);
 
 /* ------------------------------------------------------------------------
+ * Transposed copy of a 128x128-block-quantised E4M3 matrix, for FP8 Dgrad
+ * (page 1: E4M3 on all tensors, Dgrad included; page 4: weights quantised
+ * per 128x128 block).  The amax of a 128x128 block is the same after
+ * transposition, so (qT, sT) is exactly what fp8_quant_weight_128x128 would
+ * give for the transposed bf16 matrix.  Dgrad dX = dY * W is then
+ * fp8_gemm_blockscaled(a = 1x128 codes of dY, b = qT, sb = sT,
+ * FP8_BSCALE_BLOCK128).
+ *   q   E4M3 [N][K], s fp32 [N/128][K/128]   (from fp8_quant_weight_128x128)
+ *   qT  E4M3 [K][N], sT fp32 [K/128][N/128]
+ * N % 128 == 0, K % 128 == 0; q and qT 16-byte aligned.
+ * ---------------------------------------------------------------------- */
+FP8_API int fp8_transpose_128x128(const uint8_t* q, const float* s, int64_t N, int64_t K,
+                                  uint8_t* qT, float* sT, fp8_stream_t stream);
+
+/* ------------------------------------------------------------------------
  * Grouped (per-expert) block-scaled FP8 GEMM for MoE (page 4: 256 routed
  * experts; each expert processes the rows dispatched to it).  Expert e owns
  * rows [off[e], off[e+1]) of a and d and multiplies them by its own B_e:

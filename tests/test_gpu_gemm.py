@@ -150,3 +150,65 @@ def test_gemm_many_tiles_per_cluster_full_rows(fb, orc, mode, out_dtype, K):
         bound = 1e-5 * refmax + (np.abs(ref) * 2.0 ** -8 if out_dtype == torch.bfloat16 else 0.0)
         n_bad = int((err > bound).sum())
         assert n_bad == 0, "many tiles mode%d K%d rep%d: %d elements beyond the element-wise bound" % (mode, K, rep, n_bad)
+
+
+def test_tensor_core_accumulation_precision_probe(fb, orc):
+    """How many bits the tcgen05 E4M3 accumulation keeps inside one 128-element
+    K block (pages 2 and 4: Hopper's limited accumulation width is why partial
+    sums are promoted every 128 elements; nothing on the pages fixes it for
+    this part, so this is a measurement, printed, with a floor).
+
+    One product of 16 * 8 = 2^7 and 127 products of 2^-6 * 2^-7 = 2^-13, all
+    scales 1: the exact K-block sum is 2^7 + 127 * 2^-13.  An accumulator with
+    p significant bits at magnitude 2^7 keeps increments of 2^(7 - p + 1), so
+    the small terms survive only with p >= 21."""
+    K, M, N = 128, 128, 256
+    a = np.zeros((M, K), dtype=np.uint8)
+    b = np.zeros((N, K), dtype=np.uint8)
+    a[:, 0] = 0x58            # 16   = 2^4   (exponent field 11)
+    b[:, 0] = 0x50            # 8    = 2^3   (exponent field 10)
+    a[:, 1:] = 0x08           # 2^-6         (smallest normal)
+    b[:, 1:] = 0x04           # 2^-7 = 4 * 2^-9 (subnormal)
+    sa = np.ones((K // 128, M), dtype=np.float32)
+    sb = np.ones((N // 128, K // 128), dtype=np.float32)
+    d = fb.fp8_gemm_blockscaled(_dev(a), _dev(sa), _dev(b), _dev(sb), 0, torch.float32)
+    got = float(d[0, 0])
+    exact = 2.0 ** 7 + 127 * 2.0 ** -13
+    ref = orc.gemm_blockscaled(a[:1], sa[:, :1], b[:1], sb[:1, :], 0)[0, 0]
+    assert ref == exact
+    lost = exact - got
+    print("K-block accumulation probe: got %.10f exact %.10f lost %.3e (%.1f%% of the small terms)"
+          % (got, exact, lost, 100.0 * lost / (127 * 2.0 ** -13)))
+    # floor: the large term itself is exact, and at most the small terms are lost
+    assert 2.0 ** 7 <= got <= exact
+
+
+@pytest.mark.parametrize("N,K", [(128, 128), (256, 384), (896, 512)])
+def test_transpose_128x128_bit_exact(fb, N, K):
+    q = rand_codes((N, K), N + K)
+    s = rand_scales((N // 128, K // 128), N)
+    qT, sT = fb.fp8_transpose_128x128(_dev(q), _dev(s))
+    assert np.array_equal(qT.cpu().numpy(), q.T)
+    assert np.array_equal(sT.cpu().numpy().view(np.uint32), np.ascontiguousarray(s.T).view(np.uint32))
+
+
+def test_dgrad_dense_linear_sampled(fb, orc):
+    """dX = dY * W with dY [4096,7168] in 1x128 tiles and W [7168,7168] in
+    128x128 blocks: the GPU transposes W's codes; the oracle quantises W^T
+    from the bf16 values itself."""
+    d = S.dense_linear()
+    w = d["w"]
+    dy = (torch.randn((4096, 7168), generator=torch.Generator().manual_seed(3)) * 1e-3).to(torch.bfloat16)
+    qdy, sdy = fb.fp8_quant_act_1x128(dy.cuda())
+    qw, sw = fb.fp8_quant_weight_128x128(w.cuda())
+    qwT, swT = fb.fp8_transpose_128x128(qw, sw)
+    dx = fb.fp8_gemm_blockscaled(qdy, sdy, qwT, swT)
+    g = np.random.default_rng(5)
+    rows = np.unique(np.concatenate([[0, 4095], g.choice(4096, 30, replace=False)]))
+    qa, sa = orc.quant_act_1x128(S.bf16_bits(dy)[rows])
+    wtb = np.ascontiguousarray(S.bf16_bits(w).T)
+    got = to_np(dx)[rows]
+    for kb in (0, 31, 55):
+        qb, sb = orc.quant_weight_128x128(np.ascontiguousarray(wtb[kb * 128:(kb + 1) * 128]))
+        ref = orc.gemm_blockscaled(qa, sa, qb, sb, 0)
+        assert_gemm_close(got[:, kb * 128:(kb + 1) * 128], ref, True, orc, "dgrad col block %d" % kb)

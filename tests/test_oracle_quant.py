@@ -138,3 +138,18 @@ def test_zero_tile_is_finite(orc):
     q, s = orc.quant_act_1x128(_bits(x))
     assert np.all(np.isfinite(s)) and s[0, 0] == np.float32(2.0 ** -64 / 448)
     assert np.all(q[0] == 0) and q[1, 200] == 0xFE
+
+
+def test_weight_quant_of_transpose_is_transpose_of_quant(orc):
+    """A 128x128 block's max-abs does not change under transposition, so the
+    block quantisation of W^T is the transpose of W's codes and block scales
+    (what FP8 Dgrad relies on)."""
+    g = np.random.default_rng(21)
+    w = (g.standard_normal((384, 256)) * 0.02).astype(np.float32)
+    w[7, 200] = 3.0                                   # one block with an outlier
+    wb = (w.view(np.uint32) >> 16).astype(np.uint16)  # truncate to bf16 bits
+    for flags in (0, 1):
+        q, s = orc.quant_weight_128x128(wb, flags)
+        qt, st = orc.quant_weight_128x128(np.ascontiguousarray(wb.T), flags)
+        assert np.array_equal(qt, q.T)
+        assert np.array_equal(st.view(np.uint32), s.T.view(np.uint32))
