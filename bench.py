@@ -372,7 +372,13 @@ def measure_rows(F, S, dev, flush, pk):
     qdy, sdy = F.fp8_quant_act_1x128(dy)
     ms = _time(lambda: F.fp8_gemm_blockscaled(qdy, sdy, qwT, swT, 0, torch.bfloat16, d=y), reps, warm, flush, st)
     tensor_row("a8_gemm_dgrad", ms, GEMM_FLOP, "dX = dY W, 4096x7168x7168 -> bf16")
-    del x, w, qx, qw, y, qwT, dy, qdy
+    # power-of-two scales: the same GEMM with the scales applied by the tensor core
+    P = F.FP8_SCALE_POW2
+    qx2, sx2 = F.fp8_quant_act_1x128(x, flags=P)
+    qw2, sw2 = F.fp8_quant_weight_128x128(w, flags=P)
+    ms = _time(lambda: F.fp8_gemm_blockscaled_pow2(qx2, sx2, qw2, sw2, 0, torch.bfloat16, d=y), reps, warm, flush, st)
+    tensor_row("f1_gemm_dense_pow2", ms, GEMM_FLOP, "4096x7168x7168 -> bf16, pow-2 scales as UE8M0 (microscaled MMA)")
+    del x, w, qx, qw, y, qwT, dy, qdy, qx2, qw2
 
     # Wgrad rows
     d = S.wgrad()
@@ -386,7 +392,13 @@ def measure_rows(F, S, dev, flush, pk):
     ms = _time(lambda: F.fp8_gemm_blockscaled(qa, sa, qb, sb, F.FP8_BSCALE_ROW, torch.float32, d=dw),
                reps, warm, flush, st)
     tensor_row("a5_gemm_wgrad", ms, 2.0 * H * H * T, "dW = dY^T X, 7168x7168x8192 -> fp32")
-    del dy, xx, qa, qb, dw
+    P = F.FP8_SCALE_POW2
+    qa2, sa2 = F.fp8_quant_act_128x1(dy, flags=P)
+    qb2, sb2 = F.fp8_quant_act_128x1(xx, flags=P)
+    ms = _time(lambda: F.fp8_gemm_blockscaled_pow2(qa2, sa2, qb2, sb2, F.FP8_BSCALE_ROW, torch.float32, d=dw),
+               reps, warm, flush, st)
+    tensor_row("f1_gemm_wgrad_pow2", ms, 2.0 * H * H * T, "dW = dY^T X, 7168x7168x8192 -> fp32, pow-2 scales")
+    del dy, xx, qa, qb, dw, qa2, qb2
 
     # MoE up-proj
     E, k = 256, 8

@@ -267,6 +267,78 @@ FP8_DEV void umma_commit_pair(uint64_t* bar, uint16_t cta_mask) {
         : "memory");
 }
 
+// Block-scaled form (kind::mxf8f6f4, one UE8M0 scale per 32 K elements per
+// row of A and per row of B): D (+)= (sA .* A) * (sB .* B)^T over K = 32, the
+// scales read from tensor memory at sfa / sfb.  Where each scale sits (each
+// CTA's own TMEM, measured on B300):
+//   A row m (of the CTA's 128)    lane m,                    column sfa + m/32
+//   B row n, for D rows in lanes  lanes 32q .. 32q+31 (every column sfb + n/32,
+//     32q .. 32q+31                q), at lane 32q + n%32
+// and in each 32-bit word the byte chosen by the scale-ID fields of idesc.
+// Called by a whole converged warp: one lane, picked by elect.sync, issues
+// the MMA (the operands are warp-uniform, so they stay in uniform registers).
+FP8_DEV void umma_mx_e4m3_pair_elect(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc, uint32_t sfa,
+                                     uint32_t sfb, uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred pe, pa;\n\t"
+        "elect.sync _|pe, 0xffffffff;\n\t"
+        "setp.ne.b32 pa, %6, 0;\n\t"
+        "@pe tcgen05.mma.cta_group::2.kind::mxf8f6f4.block_scale.scale_vec::1X [%0], %1, %2, %3, [%4], [%5], pa;\n\t}" ::"r"(
+            d_tmem),
+        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(sfa), "r"(sfb), "r"(accumulate)
+        : "memory");
+}
+
+// The same MMA (accumulating), issued between a non-blocking probe of one or
+// two mbarrier phases and the use of the probe's result, so that the probe's
+// latency overlaps the issue of the MMA (which waits for the tensor core to
+// accept it).  Returns true when every probed phase has completed; with
+// bar1 == 0 only bar0 is probed.  Whole converged warp, as above.
+FP8_DEV bool umma_mx_e4m3_pair_probe_elect(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                           uint32_t sfa, uint32_t sfb, uint32_t bar0, uint32_t par0, uint32_t bar1,
+                                           uint32_t par1) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p0, p1, pe;\n\t"
+        "mbarrier.test_wait.parity.shared::cta.b64 p0, [%7], %8;\n\t"
+        "setp.eq.u32 p1, %9, 0;\n\t"
+        "@!p1 mbarrier.test_wait.parity.shared::cta.b64 p1, [%9], %10;\n\t"
+        "elect.sync _|pe, 0xffffffff;\n\t"
+        "@pe tcgen05.mma.cta_group::2.kind::mxf8f6f4.block_scale.scale_vec::1X [%1], %2, %3, %4, [%5], [%6], 1;\n\t"
+        "and.pred p0, p0, p1;\n\t"
+        "selp.u32 %0, 1, 0, p0;\n\t}"
+        : "=r"(ok)
+        : "r"(d_tmem), "l"(adesc), "l"(bdesc), "r"(idesc), "r"(sfa), "r"(sfb), "r"(bar0), "r"(par0), "r"(bar1),
+          "r"(par1)
+        : "memory");
+    return ok != 0;
+}
+
+// umma_commit_pair issued by one elected lane of a converged warp.
+FP8_DEV void umma_commit_pair_elect(uint64_t* bar, uint16_t cta_mask) {
+    asm volatile(
+        "{\n\t.reg .pred pe;\n\t"
+        "elect.sync _|pe, 0xffffffff;\n\t"
+        "@pe tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;\n\t}" ::"r"(
+            smem_u32(bar)),
+        "h"(cta_mask)
+        : "memory");
+}
+
+// Stores into tensor memory: thread i of the warp writes lane (base lane + i),
+// 4 or 8 consecutive 32-bit columns from `col` (taddr = lane << 16 | col).
+FP8_DEV void tmem_st_32x32b_x4(uint32_t taddr, uint32_t v0, uint32_t v1, uint32_t v2, uint32_t v3) {
+    asm volatile("tcgen05.st.sync.aligned.32x32b.x4.b32 [%0], {%1, %2, %3, %4};" ::"r"(taddr), "r"(v0), "r"(v1),
+                 "r"(v2), "r"(v3)
+                 : "memory");
+}
+FP8_DEV void tmem_st_32x32b_x8(uint32_t taddr, const uint32_t (&v)[8]) {
+    asm volatile("tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"r"(taddr),
+                 "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7])
+                 : "memory");
+}
+FP8_DEV void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
+
 // 32 lanes x 32 consecutive 32-bit columns; thread i of the warp gets lane
 // (base lane + i), columns [col, col+32).
 FP8_DEV void tmem_ld_32x32b_x32(uint32_t taddr, uint32_t (&v)[32]) {
@@ -331,6 +403,19 @@ __host__ __device__ constexpr uint32_t idesc_e4m3_f32(int M, int N) {
            | (0u << 15) | (0u << 16)     // A, B K-major
            | (uint32_t(N >> 3) << 17)    // N / 8
            | (uint32_t(M >> 4) << 24);   // M / 16
+}
+
+// Instruction descriptor, kind::mxf8f6f4 with block scaling: D = F32,
+// A = B = E4M3, both K-major, tile M x N, UE8M0 scales, scale byte 0 of each
+// 32-bit TMEM word for both A and B.
+__host__ __device__ constexpr uint32_t idesc_mx_e4m3(int M, int N) {
+    return (0u << 4)                     // B scale byte (scale ID)
+           | (0u << 7) | (0u << 10)      // A, B format: E4M3
+           | (0u << 15) | (0u << 16)     // A, B K-major
+           | (uint32_t(N >> 3) << 17)    // N / 8
+           | (1u << 23)                  // scale format: UE8M0
+           | (uint32_t(M >> 4) << 24)    // M / 16
+           | (0u << 29);                 // A scale byte (scale ID)
 }
 
 }  // namespace fp8bs

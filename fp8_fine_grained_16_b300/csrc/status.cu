@@ -3,12 +3,14 @@
 
 extern "C" int fp8bs_gemm_take_status(cudaStream_t stream);
 extern "C" int fp8bs_moe_take_status(cudaStream_t stream);
+extern "C" int fp8bs_gemm_mx_take_status(cudaStream_t stream);
 
 extern "C" int fp8_get_status(fp8_stream_t stream) {
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     const int a = fp8bs_gemm_take_status(s);
     const int b = fp8bs_moe_take_status(s);
-    return a != FP8_OK ? a : b;
+    const int c = fp8bs_gemm_mx_take_status(s);
+    return a != FP8_OK ? a : (b != FP8_OK ? b : c);
 }
 
 extern "C" const char* fp8_strerror(int code) {
@@ -22,6 +24,7 @@ extern "C" const char* fp8_strerror(int code) {
         case FP8_ERR_OFFSETS: return "expert offsets or row indices out of range";
         case FP8_ERR_DEVICE: return "no usable sm_100-family device";
         case FP8_ERR_SCRATCH: return "problem larger than the library's static scratch";
+        case FP8_ERR_SCALE: return "a scale given to the power-of-two GEMM is not a positive normal power of two";
         default: return "unknown status";
     }
 }

@@ -34,6 +34,7 @@ FP8_OUT_F32 = 1
 FP8_ERR_TIMEOUT = -5
 FP8_ERR_OFFSETS = -6
 FP8_ERR_SCRATCH = -8
+FP8_ERR_SCALE = -9
 
 _P = ctypes.c_void_p
 _I64 = ctypes.c_int64
@@ -46,6 +47,7 @@ _SIGS = {
     "fp8_quant_act_128x1": [_P, _I64, _I64, _I64, _P, _P, _U32, _P],
     "fp8_quant_weight_128x128": [_P, _I64, _I64, _I64, _P, _P, _U32, _P],
     "fp8_gemm_blockscaled": [_P, _P, _P, _P, _I, _P, _I, _I64, _I64, _I64, _P],
+    "fp8_gemm_blockscaled_pow2": [_P, _P, _P, _P, _I, _P, _I, _I64, _I64, _I64, _P],
     "fp8_transpose_128x128": [_P, _P, _I64, _I64, _P, _P, _P],
     "fp8_grouped_gemm_blockscaled": [_P, _P, _P, _P, _P, _I, _I64, _I64, _I64, _P, _P],
     "fp8_moe_route_topk": [_P, _I64, _I, _I, _P, _P, _P, _P, _P, _P, _P],
@@ -169,6 +171,22 @@ def fp8_gemm_blockscaled(a, sa, b, sb, b_scale_mode: int = FP8_BSCALE_BLOCK128, 
     if d is None:
         d = torch.empty((M, N), dtype=torch.float32 if d_dtype == FP8_OUT_F32 else torch.bfloat16, device=a.device)
     _check("fp8_gemm_blockscaled", lib.fp8_gemm_blockscaled(
+        _ptr(a, torch.uint8, "a"), _ptr(sa, torch.float32, "sa"), _ptr(b, torch.uint8, "b"),
+        _ptr(sb, torch.float32, "sb"), b_scale_mode, _ptr(d, None, "d"), d_dtype, M, N, K, _stream(stream)))
+    return d
+
+
+def fp8_gemm_blockscaled_pow2(a, sa, b, sb, b_scale_mode: int = FP8_BSCALE_BLOCK128, out_dtype=torch.bfloat16,
+                              d=None, stream=None) -> torch.Tensor:
+    """As fp8_gemm_blockscaled, for power-of-two scales applied by the tensor core."""
+    M, K = a.shape
+    N = b.shape[0]
+    if b.shape[1] != K:
+        raise ValueError("a and b disagree on K")
+    d_dtype = FP8_OUT_F32 if out_dtype == torch.float32 else FP8_OUT_BF16
+    if d is None:
+        d = torch.empty((M, N), dtype=torch.float32 if d_dtype == FP8_OUT_F32 else torch.bfloat16, device=a.device)
+    _check("fp8_gemm_blockscaled_pow2", lib.fp8_gemm_blockscaled_pow2(
         _ptr(a, torch.uint8, "a"), _ptr(sa, torch.float32, "sa"), _ptr(b, torch.uint8, "b"),
         _ptr(sb, torch.float32, "sb"), b_scale_mode, _ptr(d, None, "d"), d_dtype, M, N, K, _stream(stream)))
     return d

@@ -61,7 +61,8 @@ enum fp8_status {
     FP8_ERR_TIMEOUT = -5,    /* a kernel's bounded pipeline wait expired (device status) */
     FP8_ERR_OFFSETS = -6,    /* expert offsets not monotone or out of range (device status) */
     FP8_ERR_DEVICE = -7,     /* no usable sm_100-family device */
-    FP8_ERR_SCRATCH = -8     /* problem larger than the library's static scratch */
+    FP8_ERR_SCRATCH = -8,    /* problem larger than the library's static scratch */
+    FP8_ERR_SCALE = -9       /* a scale is not a positive normal power of two (device status) */
 };
 
 /* flags of the quantisers */
@@ -148,6 +149,26 @@ FP8_API int fp8_gemm_blockscaled(const uint8_t* a, const float* sa,
                                  const uint8_t* b, const float* sb, int b_scale_mode,
                                  void* d, int d_dtype, int64_t M, int64_t N, int64_t K,
                                  fp8_stream_t stream);
+
+/* ------------------------------------------------------------------------
+ * The same GEMM for power-of-two scales (the quantisers' FP8_SCALE_POW2
+ * mode; page 2: integral-power-of-2 scaling factors), with the scales applied
+ * by the tensor core (page 3: fine-grained tiles match microscaling, which
+ * Blackwell tensor cores support; page 2: tensor cores that take the scaling
+ * factors).  Each scale 2^e becomes a UE8M0 scale factor of the block-scaled
+ * tcgen05 MMA, repeated over the four 32-element K groups of its 128-element
+ * K block, and D accumulates in fp32 in tensor memory over the whole K:
+ *   D[m][n] = sum_k (sA[k/128][m] * A[m][k]) * (sB(n, k/128) * B[n][k])
+ * which is the block-promoted sum of fp8_gemm_blockscaled up to fp32
+ * rounding order.  Arguments, layouts and limits are those of
+ * fp8_gemm_blockscaled.  Every scale read (rows < M, columns < N) must be a
+ * positive normal power of two; the kernel records FP8_ERR_SCALE in the
+ * device status otherwise, and the result is then undefined.
+ * ---------------------------------------------------------------------- */
+FP8_API int fp8_gemm_blockscaled_pow2(const uint8_t* a, const float* sa,
+                                      const uint8_t* b, const float* sb, int b_scale_mode,
+                                      void* d, int d_dtype, int64_t M, int64_t N, int64_t K,
+                                      fp8_stream_t stream);
 
 /* ------------------------------------------------------------------------
  * Transposed copy of a 128x128-block-quantised E4M3 matrix, for FP8 Dgrad
