@@ -436,7 +436,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     if (lane == 0) mbar_arrive(&empty[stage]);
                 }
 
-                auto scale_chunk = [&](int c, const uint32_t (&v)[32]) {
+                auto scale_chunk = [&](int c, const uint32_t* v) {
                     if constexpr (BMODE == 0) {
 #pragma unroll
                         for (int i = 0; i < 16; ++i)
@@ -460,24 +460,24 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                 };
 
-                // 32 columns at a time: a TMEM load round trip is short, and one
-                // 32-register batch leaves the accumulators room
+                // 64 columns at a time (two loads per K block): the second load's
+                // wait frees the accumulator, and one 64-register batch beside
+                // the 128 accumulators fits the promotion's register share
                 const uint32_t tcol = tmem_base + t_lane + buf * BN + half * kHalf;
-                uint32_t v[32];
-#pragma unroll
-                for (int c = 0; c < 3; ++c) {
-                    tmem_ld_32x32b_x32(tcol + 32 * c, v);
-                    tmem_wait_ld_regs(v);
-                    scale_chunk(c, v);
-                }
-                tmem_ld_32x32b_x32(tcol + 96, v);
-                tmem_wait_ld_regs(v);
+                uint32_t v[64];
+                tmem_ld_32x32b_x64(tcol, v);
+                tmem_wait_ld_regs64(v);
+                scale_chunk(0, v);
+                scale_chunk(1, v + 32);
+                tmem_ld_32x32b_x64(tcol + 64, v);
+                tmem_wait_ld_regs64(v);
                 tc_fence_before();
                 __syncwarp();
                 // all of P_kb is in registers: accumulator `buf` is free for K
                 // block g + 2 (on the leader's full[])
                 if (lane == 0) mbar_arrive_cluster(full0 + ((g + 2) % STAGES) * 8);
-                scale_chunk(3, v);
+                scale_chunk(2, v);
+                scale_chunk(3, v + 32);
                 if constexpr (BMODE == 1) {
                     __syncwarp();
                     if (lane == 0) mbar_arrive(&empty[stage]);
