@@ -364,6 +364,13 @@ def measure_rows(F, S, dev, flush, pk):
     hbm_row("a3_quant_weight_128x128", ms, N * K * 3 + (N // 128) * (K // 128) * 4, "W [7168,7168]")
     ms = _time(lambda: F.fp8_gemm_blockscaled(qx, sx, qw, sw, 0, torch.bfloat16, d=y), reps, warm, flush, st)
     tensor_row("a4_gemm_dense", ms, GEMM_FLOP, "4096x7168x7168 -> bf16")
+    # the same GEMM quantising D in its epilogue (1x128 tiles along N) for the next GEMM;
+    # unfused, that is the bf16-out GEMM plus a 1x128 quantiser pass over a [4096,7168] bf16 tensor
+    q8, s8 = F.fp8_gemm_blockscaled_q8(qx, sx, qw, sw)
+    ms = _time(lambda: F.fp8_gemm_blockscaled_q8(qx, sx, qw, sw, 0, 0, q8, s8), reps, warm, flush, st)
+    tensor_row("f2_gemm_dense_q8", ms, GEMM_FLOP, "4096x7168x7168 -> E4M3 + 1x128 scales (quantised in the epilogue)",
+               dict(unfused_ms=round(out["a4_gemm_dense"]["ms"] + out["a1_quant_act_1x128"]["ms"], 5)))
+    del q8, s8
     # Dgrad: dX = dY W from the transposed 128x128-block codes of W
     qwT, swT = F.fp8_transpose_128x128(qw, sw)
     ms = _time(lambda: F.fp8_transpose_128x128(qw, sw, qwT, swT), reps, warm, flush, st)

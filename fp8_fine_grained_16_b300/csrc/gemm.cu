@@ -73,13 +73,18 @@ static_assert(kSaRegion % 128 == 0 && kSaRegion >= kSaBox * 4 && (kSbHalf0 * 4) 
 struct GemmArgs {
     const float* sa;
     const float* sb;
-    void* d;
+    void* d;                 // bf16 / fp32 output, or the E4M3 codes of D
     const int32_t* off;      // grouped only
     int64_t M;               // dense: rows of A / D; grouped: total_rows
     int64_t N;
     int64_t K;
     int E;                   // grouped only
+    float* s_out;            // E4M3 output: 1x128 scales of D, [N/128][M]
+    uint32_t flags;          // E4M3 output: FP8_SCALE_POW2
 };
+
+// Output forms of the GEMM.
+constexpr int kOutBF16 = 0, kOutF32 = 1, kOutE4M3 = 2;
 
 struct Tile {
     int64_t row0;            // first row of the tile (global row index)
@@ -184,7 +189,7 @@ struct GroupedPairSched {
     }
 };
 
-template <int BN, int STAGES, int BMODE, bool OUT_F32, bool GROUPED>
+template <int BN, int STAGES, int BMODE, int OUT, bool GROUPED>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                      const __grid_constant__ CUtensorMap tmSA, const __grid_constant__ CUtensorMap tmSB,
@@ -489,7 +494,30 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int64_t m = t.row0 + r;
             const int64_t ncol0 = int64_t(t.n0) + half * kHalf;
             if (ncol0 < args.N && m < t.row_end && m < args.M) {
-                if constexpr (OUT_F32) {
+                if constexpr (OUT == kOutE4M3) {
+                    // The thread holds row m, columns ncol0 .. ncol0+127 of D in
+                    // fp32: exactly one 1x128 activation tile of the next GEMM
+                    // (its K runs along this GEMM's N).  Quantise it as the
+                    // 1x128 quantiser does: fp32 amax, scale, x*inv, E4M3.
+                    float amax = 0.0f;
+#pragma unroll
+                    for (int i = 0; i < kHalf / 2; ++i) amax = fmaxf(amax, fmaxf(fabsf(acc[i].x), fabsf(acc[i].y)));
+                    float inv;
+                    const float sc = tile_scale(amax, (args.flags & FP8_SCALE_POW2) != 0, inv);
+                    uint8_t* dst = reinterpret_cast<uint8_t*>(args.d) + m * args.N + ncol0;
+#pragma unroll
+                    for (int i = 0; i < kHalf / 2; i += 8) {
+                        uint32_t w[4];
+#pragma unroll
+                        for (int j = 0; j < 4; ++j)
+                            w[j] = cvt_e4m3x2(__fmul_rn(acc[i + 2 * j].x, inv), __fmul_rn(acc[i + 2 * j].y, inv)) |
+                                   (cvt_e4m3x2(__fmul_rn(acc[i + 2 * j + 1].x, inv),
+                                               __fmul_rn(acc[i + 2 * j + 1].y, inv))
+                                    << 16);
+                        *reinterpret_cast<uint4*>(dst + 2 * i) = make_uint4(w[0], w[1], w[2], w[3]);
+                    }
+                    args.s_out[(ncol0 / 128) * args.M + m] = sc;
+                } else if constexpr (OUT == kOutF32) {
                     float* dst = reinterpret_cast<float*>(args.d) + m * args.N + ncol0;
 #pragma unroll
                     for (int i = 0; i < kHalf / 2; i += 2)
@@ -524,11 +552,11 @@ __global__ void __launch_bounds__(kThreads, 1)
 // ---------------------------------------------------------------- host side
 constexpr int kBN = 256;
 
-template <int BN, int STAGES, int BMODE, bool OUT_F32, bool GROUPED>
+template <int BN, int STAGES, int BMODE, int OUT, bool GROUPED>
 static int launch_pair(const CUtensorMap& ma, const CUtensorMap& mb, const CUtensorMap& msa, const CUtensorMap& msb,
                        const GemmArgs& args, int sms, cudaStream_t stream) {
     using L = PairLayout<BN, STAGES, BMODE, GROUPED>;
-    auto kern = gemm_pair_kernel<BN, STAGES, BMODE, OUT_F32, GROUPED>;
+    auto kern = gemm_pair_kernel<BN, STAGES, BMODE, OUT, GROUPED>;
     static bool attr_set = false;
     if (!attr_set) {
         if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kDynSmem) != cudaSuccess)
@@ -594,16 +622,47 @@ extern "C" int fp8_gemm_blockscaled(const uint8_t* a, const float* sa, const uin
         !make_scale_map(&msa, sa, M * (K / 128), kSaBox) ||
         !make_scale_map(&msb, sb, nsb, b_scale_mode == FP8_BSCALE_ROW ? kBN : kSbBox0))
         return FP8_ERR_CUDA;
-    GemmArgs args{sa, sb, d, nullptr, M, N, K, 0};
+    GemmArgs args{sa, sb, d, nullptr, M, N, K, 0, nullptr, 0u};
     const int64_t pair_tiles = ((M + 2 * BM - 1) / (2 * BM)) * ((N + kBN - 1) / kBN);
     const int grid_sms = int(2 * pair_tiles < sms ? 2 * pair_tiles : sms);
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     if (b_scale_mode == FP8_BSCALE_BLOCK128) {
-        if (d_dtype == FP8_OUT_BF16) return launch_pair<kBN, kPairStages, 0, false, false>(ma, mb, msa, msb, args, grid_sms, s);
-        return launch_pair<kBN, kPairStages, 0, true, false>(ma, mb, msa, msb, args, grid_sms, s);
+        if (d_dtype == FP8_OUT_BF16) return launch_pair<kBN, kPairStages, 0, kOutBF16, false>(ma, mb, msa, msb, args, grid_sms, s);
+        return launch_pair<kBN, kPairStages, 0, kOutF32, false>(ma, mb, msa, msb, args, grid_sms, s);
     }
-    if (d_dtype == FP8_OUT_BF16) return launch_pair<kBN, kPairStages, 1, false, false>(ma, mb, msa, msb, args, grid_sms, s);
-    return launch_pair<kBN, kPairStages, 1, true, false>(ma, mb, msa, msb, args, grid_sms, s);
+    if (d_dtype == FP8_OUT_BF16) return launch_pair<kBN, kPairStages, 1, kOutBF16, false>(ma, mb, msa, msb, args, grid_sms, s);
+    return launch_pair<kBN, kPairStages, 1, kOutF32, false>(ma, mb, msa, msb, args, grid_sms, s);
+}
+
+extern "C" int fp8_gemm_blockscaled_q8(const uint8_t* a, const float* sa, const uint8_t* b, const float* sb,
+                                       int b_scale_mode, uint8_t* q_out, float* s_out, uint32_t flags, int64_t M,
+                                       int64_t N, int64_t K, fp8_stream_t stream) {
+    if (!a || !sa || !b || !sb || !q_out || !s_out || M <= 0 || N <= 0 || K <= 0) return FP8_ERR_ARG;
+    if ((b_scale_mode != FP8_BSCALE_BLOCK128 && b_scale_mode != FP8_BSCALE_ROW) || (flags & ~FP8_SCALE_POW2))
+        return FP8_ERR_ARG;
+    if (K % 128 || N % 128) return FP8_ERR_SHAPE;
+    if (M > (int64_t(1) << 31) - 1 || N > (int64_t(1) << 31) - 1 || K > (int64_t(1) << 31) - 1) return FP8_ERR_SHAPE;
+    if (!aligned16(a) || !aligned16(b) || !aligned16(q_out) || !aligned16(sa) || !aligned16(sb) ||
+        (reinterpret_cast<uintptr_t>(s_out) & 3u))
+        return FP8_ERR_ALIGN;
+    if (M * (K / 128) >= (int64_t(1) << 31) || M * (N / 128) >= (int64_t(1) << 31) ||
+        (b_scale_mode == FP8_BSCALE_ROW && N * (K / 128) >= (int64_t(1) << 31)))
+        return FP8_ERR_SHAPE;
+    const int sms = device_sms();
+    if (sms <= 0) return FP8_ERR_DEVICE;
+    CUtensorMap ma, mb, msa, msb;
+    const int64_t nsb = b_scale_mode == FP8_BSCALE_ROW ? N * (K / 128) : (N / 128) * (K / 128);
+    if (!make_operand_map(&ma, a, M, K, BM, 1, false) || !make_operand_map(&mb, b, N, K, kBN / 2, 1, false) ||
+        !make_scale_map(&msa, sa, M * (K / 128), kSaBox) ||
+        !make_scale_map(&msb, sb, nsb, b_scale_mode == FP8_BSCALE_ROW ? kBN : kSbBox0))
+        return FP8_ERR_CUDA;
+    GemmArgs args{sa, sb, q_out, nullptr, M, N, K, 0, s_out, flags};
+    const int64_t pair_tiles = ((M + 2 * BM - 1) / (2 * BM)) * ((N + kBN - 1) / kBN);
+    const int grid_sms = int(2 * pair_tiles < sms ? 2 * pair_tiles : sms);
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if (b_scale_mode == FP8_BSCALE_BLOCK128)
+        return launch_pair<kBN, kPairStages, 0, kOutE4M3, false>(ma, mb, msa, msb, args, grid_sms, s);
+    return launch_pair<kBN, kPairStages, 1, kOutE4M3, false>(ma, mb, msa, msb, args, grid_sms, s);
 }
 
 extern "C" int fp8_grouped_gemm_blockscaled(const uint8_t* a, const float* sa, const uint8_t* b, const float* sb,
@@ -628,8 +687,8 @@ extern "C" int fp8_grouped_gemm_blockscaled(const uint8_t* a, const float* sa, c
         !make_scale_map(&msa, sa, total_rows * (K / 128), kSaBox) ||
         !make_scale_map(&msb, sb, int64_t(E) * (N / 128) * (K / 128), kSbBox0))
         return FP8_ERR_CUDA;
-    GemmArgs args{sa, sb, d, expert_offsets, total_rows, N, K, E};
-    return launch_pair<kBN, kPairStages, 0, false, true>(ma, mb, msa, msb, args, sms, reinterpret_cast<cudaStream_t>(stream));
+    GemmArgs args{sa, sb, d, expert_offsets, total_rows, N, K, E, nullptr, 0u};
+    return launch_pair<kBN, kPairStages, 0, kOutBF16, true>(ma, mb, msa, msb, args, sms, reinterpret_cast<cudaStream_t>(stream));
 }
 
 extern "C" int fp8_selftest_wait_timeout(uint64_t timeout_ns, fp8_stream_t stream) {

@@ -48,6 +48,7 @@ _SIGS = {
     "fp8_quant_weight_128x128": [_P, _I64, _I64, _I64, _P, _P, _U32, _P],
     "fp8_gemm_blockscaled": [_P, _P, _P, _P, _I, _P, _I, _I64, _I64, _I64, _P],
     "fp8_gemm_blockscaled_pow2": [_P, _P, _P, _P, _I, _P, _I, _I64, _I64, _I64, _P],
+    "fp8_gemm_blockscaled_q8": [_P, _P, _P, _P, _I, _P, _P, _U32, _I64, _I64, _I64, _P],
     "fp8_transpose_128x128": [_P, _P, _I64, _I64, _P, _P, _P],
     "fp8_grouped_gemm_blockscaled": [_P, _P, _P, _P, _P, _I, _I64, _I64, _I64, _P, _P],
     "fp8_moe_route_topk": [_P, _I64, _I, _I, _P, _P, _P, _P, _P, _P, _P],
@@ -190,6 +191,23 @@ def fp8_gemm_blockscaled_pow2(a, sa, b, sb, b_scale_mode: int = FP8_BSCALE_BLOCK
         _ptr(a, torch.uint8, "a"), _ptr(sa, torch.float32, "sa"), _ptr(b, torch.uint8, "b"),
         _ptr(sb, torch.float32, "sb"), b_scale_mode, _ptr(d, None, "d"), d_dtype, M, N, K, _stream(stream)))
     return d
+
+
+def fp8_gemm_blockscaled_q8(a, sa, b, sb, b_scale_mode: int = FP8_BSCALE_BLOCK128, flags: int = 0,
+                            q_out=None, s_out=None, stream=None):
+    """D = block-scaled a x b^T, quantised in the epilogue per 1x128 tile along N:
+    (q u8 [M, N], s f32 [N/128, M]), the layout fp8_quant_act_1x128 produces."""
+    M, K = a.shape
+    N = b.shape[0]
+    if b.shape[1] != K:
+        raise ValueError("a and b disagree on K")
+    q_out = torch.empty((M, N), dtype=torch.uint8, device=a.device) if q_out is None else q_out
+    s_out = torch.empty((N // 128, M), dtype=torch.float32, device=a.device) if s_out is None else s_out
+    _check("fp8_gemm_blockscaled_q8", lib.fp8_gemm_blockscaled_q8(
+        _ptr(a, torch.uint8, "a"), _ptr(sa, torch.float32, "sa"), _ptr(b, torch.uint8, "b"),
+        _ptr(sb, torch.float32, "sb"), b_scale_mode, _ptr(q_out, torch.uint8, "q_out"),
+        _ptr(s_out, torch.float32, "s_out"), flags, M, N, K, _stream(stream)))
+    return q_out, s_out
 
 
 def fp8_transpose_128x128(q, s, qT=None, sT=None, stream=None):

@@ -151,6 +151,26 @@ FP8_API int fp8_gemm_blockscaled(const uint8_t* a, const float* sa,
                                  fp8_stream_t stream);
 
 /* ------------------------------------------------------------------------
+ * The block-scaled GEMM with its result quantised in the epilogue (page 2:
+ * BF16 activations are read from HBM, quantised and written back, only to
+ * be read again for the next MMA; quantising the producer's output where it
+ * is formed removes that round trip).  D is computed exactly as by
+ * fp8_gemm_blockscaled (fp32, promoted per 128-element K block) and, instead
+ * of being stored, quantised per 1x128 tile along N (amax in fp32, scale by
+ * flags, codes E4M3(fp32(D * inv))), i.e. the output of
+ * fp8_quant_act_1x128 applied to the fp32 D, ready to be the A operand of
+ * the next GEMM (whose K runs along this N).
+ *   a, sa, b, sb, b_scale_mode, M, N, K   as fp8_gemm_blockscaled
+ *   q_out  E4M3 [M][N], 16-byte aligned
+ *   s_out  fp32 [N/128][M]
+ *   flags  0 or FP8_SCALE_POW2
+ * ---------------------------------------------------------------------- */
+FP8_API int fp8_gemm_blockscaled_q8(const uint8_t* a, const float* sa,
+                                    const uint8_t* b, const float* sb, int b_scale_mode,
+                                    uint8_t* q_out, float* s_out, uint32_t flags,
+                                    int64_t M, int64_t N, int64_t K, fp8_stream_t stream);
+
+/* ------------------------------------------------------------------------
  * The same GEMM for power-of-two scales (the quantisers' FP8_SCALE_POW2
  * mode; page 2: integral-power-of-2 scaling factors), with the scales applied
  * by the tensor core (page 3: fine-grained tiles match microscaling, which

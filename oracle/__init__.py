@@ -74,6 +74,7 @@ def _declare(L):
     L.orc_tile_scale.restype = ctypes.c_float
     L.orc_tile_scale.argtypes = [ctypes.c_float, U32, ctypes.POINTER(ctypes.c_float)]
     L.orc_quant_act_1x128.argtypes = [P, I64, I64, I64, P, P, U32]
+    L.orc_quant_act_1x128_f32.argtypes = [P, I64, I64, P, P, U32]
     L.orc_quant_act_128x1.argtypes = [P, I64, I64, I64, P, P, U32]
     L.orc_quant_weight_128x128.argtypes = [P, I64, I64, I64, P, P, U32]
     L.orc_gemm_blockscaled_at.argtypes = [P, P, P, P, INT, I64, I64, I64, P, I64, P, I64, P]
@@ -155,6 +156,18 @@ def quant_act_1x128(x, flags: int = 0):
     q = np.empty((M, K), np.uint8)
     s = np.empty((K // 128, M), np.float32)
     lib().orc_quant_act_1x128(_p(x), M, K, K, _p(q), _p(s), flags)
+    return q, s
+
+
+def quant_act_1x128_f32(x, flags: int = 0):
+    """x float32 [M, K] -> (q uint8 [M, K], s float32 [K/128, M]): the 1x128
+    tile rule on fp32 values (the quantisation a GEMM epilogue applies)."""
+    x = _c(x, np.float32)
+    M, K = x.shape
+    assert K % 128 == 0
+    q = np.empty((M, K), np.uint8)
+    s = np.empty((K // 128, M), np.float32)
+    lib().orc_quant_act_1x128_f32(_p(x), M, K, _p(q), _p(s), flags)
     return q, s
 
 

@@ -195,6 +195,28 @@ void orc_quant_act_1x128(const uint16_t* x, int64_t M, int64_t K, int64_t ldx,
     }
 }
 
+/* 1x128 tiles of an fp32 matrix: x fp32 [M][K], q [M][K], s [K/128][M].
+ * The same tile rule as above on fp32 values; it defines the quantisation of
+ * a GEMM result in the producer's epilogue (p2: quantising where the BF16
+ * activation is formed instead of re-reading it from HBM). */
+void orc_quant_act_1x128_f32(const float* x, int64_t M, int64_t K, uint8_t* q, float* s, uint32_t flags) {
+    int64_t nkb = K / 128;
+#pragma omp parallel for schedule(static)
+    for (int64_t m = 0; m < M; ++m) {
+        for (int64_t kb = 0; kb < nkb; ++kb) {
+            const float* t = x + m * K + kb * 128;
+            float amax = 0.0f;
+            for (int i = 0; i < 128; ++i) {
+                float v = fabsf(t[i]);
+                if (v > amax) amax = v;
+            }
+            float inv;
+            s[kb * M + m] = orc_tile_scale(amax, flags, &inv);
+            for (int i = 0; i < 128; ++i) q[m * K + kb * 128 + i] = quant_one(t[i], inv);
+        }
+    }
+}
+
 /* 128x1 activation tiles along tokens, output transposed:
  * x bf16 [T][ldx] (H used columns), qT [H][T], s [T/128][H]. */
 void orc_quant_act_128x1(const uint16_t* x, int64_t T, int64_t H, int64_t ldx,

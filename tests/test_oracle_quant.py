@@ -153,3 +153,47 @@ def test_weight_quant_of_transpose_is_transpose_of_quant(orc):
         qt, st = orc.quant_weight_128x128(np.ascontiguousarray(wb.T), flags)
         assert np.array_equal(qt, q.T)
         assert np.array_equal(st.view(np.uint32), s.T.view(np.uint32))
+
+
+# ---- the 1x128 tile rule on fp32 values (the quantising GEMM epilogue)
+@pytest.mark.parametrize("flags", [0, 1])
+def test_f32_tile_quant_equals_bf16_tile_quant_on_bf16_values(orc, flags):
+    """On values that bf16 represents exactly the fp32 form must give the
+    pinned bf16 quantiser's codes and scales bit for bit."""
+    x = _rand_bf16((37, 512), 11, scale=3.0)
+    q1, s1 = orc.quant_act_1x128(_bits(x), flags)
+    q2, s2 = orc.quant_act_1x128_f32(x.float().numpy(), flags)
+    assert np.array_equal(q1, q2)
+    assert np.array_equal(s1.view(np.uint32), s2.view(np.uint32))
+
+
+def _e4m3_table(orc):
+    return orc.e4m3_decode(np.arange(256, dtype=np.uint8))
+
+
+@pytest.mark.parametrize("flags", [0, 1])
+def test_f32_tile_quant_follows_the_tile_rule(orc, flags):
+    """fp32 values that are not bf16 values, over ~60 binades: (default) each
+    tile's max-abs element codes to +-448; (pow2) the scale is a power of two
+    with 224*s < amax <= 448*s; every element dequantises within half an E4M3
+    step (2^-4 relative for normals, 2^-10 * s absolute for subnormals)."""
+    g = np.random.default_rng(3)
+    x = (g.standard_t(3, size=(64, 384)) * np.exp(g.uniform(-20, 20, size=(64, 1)))).astype(np.float32)
+    q, s = orc.quant_act_1x128_f32(x, flags)
+    tab = _e4m3_table(orc)
+    st = np.repeat(s.T.astype(np.float64), 128, axis=1)          # [M, K]: the scale of each element's tile
+    deq = tab[q] * st
+    xt = x.reshape(64, 3, 128)
+    amax = np.abs(xt).max(axis=2)                                 # [M, K/128]
+    if flags == 0:
+        arg = np.abs(xt).argmax(axis=2)
+        codes = np.take_along_axis(q.reshape(64, 3, 128), arg[..., None], axis=2)[..., 0]
+        assert np.all((codes == 0x7E) | (codes == 0xFE))
+    else:
+        sm = s.T.astype(np.float64)
+        m, e = np.frexp(sm)
+        assert np.all(m == 0.5)
+        assert np.all(224.0 * sm < amax) and np.all(amax <= 448.0 * sm)
+    err = np.abs(deq - x.astype(np.float64))
+    bound = 2.0 ** -4 * np.abs(x.astype(np.float64)) * (1 + 1e-6) + 2.0 ** -10 * st
+    assert np.all(err <= bound)
