@@ -443,6 +443,13 @@ def measure_rows(F, S, dev, flush, pk):
     qh, sh = F.fp8_quant_act_1x128(h)
     ms = _time(lambda: F.fp8_quant_act_1x128(h, qh, sh), reps, warm, flush, st)
     hbm_row("a1_quant_act_1x128_moe_down", ms, R * Kd * 3 + R * (Kd // 128) * 4, "h [32768,2048]")
+    # the same input formed from the up-projection output: SwiGLU fused with power-of-two 1x128 quantisation
+    yup = torch.randn((R, 2 * Kd), generator=torch.Generator(device=dev).manual_seed(5), device=dev).to(torch.bfloat16)
+    qg, sg = F.fp8_swiglu_quant_1x128(yup, Kd)
+    ms = _time(lambda: F.fp8_swiglu_quant_1x128(yup, Kd, qg, sg), reps, warm, flush, st)
+    hbm_row("f4_swiglu_quant_1x128_pow2", ms, R * 2 * Kd * 2 + R * Kd + R * (Kd // 128) * 4,
+            "[32768, 2 x 2048] bf16 -> h = SiLU(gate)*up as E4M3 + pow-2 scales")
+    del yup, qg, sg
     wst = S.expert_weights(1, E, Nd, Kd, device=dev)
     qwd, swd = F.fp8_quant_weight_128x128(wst)
     del wst

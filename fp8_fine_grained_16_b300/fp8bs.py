@@ -49,6 +49,7 @@ _SIGS = {
     "fp8_gemm_blockscaled": [_P, _P, _P, _P, _I, _P, _I, _I64, _I64, _I64, _P],
     "fp8_gemm_blockscaled_pow2": [_P, _P, _P, _P, _I, _P, _I, _I64, _I64, _I64, _P],
     "fp8_gemm_blockscaled_q8": [_P, _P, _P, _P, _I, _P, _P, _U32, _I64, _I64, _I64, _P],
+    "fp8_swiglu_quant_1x128": [_P, _I64, _I64, _I64, _P, _P, _U32, _P],
     "fp8_transpose_128x128": [_P, _P, _I64, _I64, _P, _P, _P],
     "fp8_grouped_gemm_blockscaled": [_P, _P, _P, _P, _P, _I, _I64, _I64, _I64, _P, _P],
     "fp8_moe_route_topk": [_P, _I64, _I, _I, _P, _P, _P, _P, _P, _P, _P],
@@ -191,6 +192,20 @@ def fp8_gemm_blockscaled_pow2(a, sa, b, sb, b_scale_mode: int = FP8_BSCALE_BLOCK
         _ptr(a, torch.uint8, "a"), _ptr(sa, torch.float32, "sa"), _ptr(b, torch.uint8, "b"),
         _ptr(sb, torch.float32, "sb"), b_scale_mode, _ptr(d, None, "d"), d_dtype, M, N, K, _stream(stream)))
     return d
+
+
+def fp8_swiglu_quant_1x128(y: torch.Tensor, I: int, q=None, s=None, flags: int = FP8_SCALE_POW2, stream=None):
+    """y bf16 [R, >= 2I] (gate | up; row stride may exceed the width) -> SwiGLU
+    quantised per 1x128 tile: (q u8 [R, I], s f32 [I/128, R]).  Power-of-two
+    scales by default."""
+    R, _, ldy = _rows(y, "y")
+    if y.dtype != torch.bfloat16 or not y.is_cuda:
+        raise TypeError("y must be a CUDA bf16 tensor")
+    q = torch.empty((R, I), dtype=torch.uint8, device=y.device) if q is None else q
+    s = torch.empty((I // 128, R), dtype=torch.float32, device=y.device) if s is None else s
+    _check("fp8_swiglu_quant_1x128", lib.fp8_swiglu_quant_1x128(
+        y.data_ptr(), R, I, ldy, _ptr(q, torch.uint8, "q"), _ptr(s, torch.float32, "s"), flags, _stream(stream)))
+    return q, s
 
 
 def fp8_gemm_blockscaled_q8(a, sa, b, sb, b_scale_mode: int = FP8_BSCALE_BLOCK128, flags: int = 0,

@@ -128,6 +128,26 @@ FP8_API int fp8_quant_weight_128x128(const uint16_t* w, int64_t N, int64_t K, in
                                      uint8_t* q, float* s, uint32_t flags, fp8_stream_t stream);
 
 /* ------------------------------------------------------------------------
+ * SwiGLU fused with 1x128 quantisation of its output: the input of the MoE
+ * down-projection (page 2: that activation's scaling factors are integral
+ * powers of 2, so flags = FP8_SCALE_POW2 is its natural setting; page 4:
+ * 1x128 tiles).  For each row r and column j < I:
+ *   h = (g * sigma(g)) * u,  g = y[r][j], u = y[r][I + j],
+ *   sigma(g) = 1 / (1 + e^-g)
+ * each step one fp32 operation, with e^x by Cody-Waite reduction and a
+ * degree-7 Taylor polynomial (within 1 ulp), so h is a fixed function of the
+ * inputs; then the 1x128 tile rule of fp8_quant_act_1x128 on the fp32 h.
+ * h is never written to memory.
+ *   y  bf16 [R][ldy]: gate in columns 0..I-1, up in I..2I-1; ldy >= 2I,
+ *      ldy % 8 == 0
+ *   q  E4M3 [R][I]
+ *   s  fp32 [I/128][R]
+ * I % 128 == 0.
+ * ---------------------------------------------------------------------- */
+FP8_API int fp8_swiglu_quant_1x128(const uint16_t* y, int64_t R, int64_t I, int64_t ldy,
+                                   uint8_t* q, float* s, uint32_t flags, fp8_stream_t stream);
+
+/* ------------------------------------------------------------------------
  * Block-scaled FP8 GEMM (pages 2 and 3: partial sums are accumulated on the
  * tensor cores over a K interval, then multiplied by the scaling factors and
  * added into FP32; page 4: the interval is 128 elements).

@@ -75,6 +75,10 @@ def _declare(L):
     L.orc_tile_scale.argtypes = [ctypes.c_float, U32, ctypes.POINTER(ctypes.c_float)]
     L.orc_quant_act_1x128.argtypes = [P, I64, I64, I64, P, P, U32]
     L.orc_quant_act_1x128_f32.argtypes = [P, I64, I64, P, P, U32]
+    L.orc_exp_cw.restype = ctypes.c_float
+    L.orc_exp_cw.argtypes = [ctypes.c_float]
+    L.orc_swiglu_f32.argtypes = [P, I64, I64, I64, P]
+    L.orc_swiglu_quant_1x128.argtypes = [P, I64, I64, I64, P, P, U32]
     L.orc_quant_act_128x1.argtypes = [P, I64, I64, I64, P, P, U32]
     L.orc_quant_weight_128x128.argtypes = [P, I64, I64, I64, P, P, U32]
     L.orc_gemm_blockscaled_at.argtypes = [P, P, P, P, INT, I64, I64, I64, P, I64, P, I64, P]
@@ -168,6 +172,32 @@ def quant_act_1x128_f32(x, flags: int = 0):
     q = np.empty((M, K), np.uint8)
     s = np.empty((K // 128, M), np.float32)
     lib().orc_quant_act_1x128_f32(_p(x), M, K, _p(q), _p(s), flags)
+    return q, s
+
+
+def exp_cw(x) -> np.ndarray:
+    """The oracle's fp32 e^x (Cody-Waite reduction, degree-7 Taylor)."""
+    x = _c(x, np.float32)
+    return np.array([lib().orc_exp_cw(float(v)) for v in x.ravel()], dtype=np.float32).reshape(x.shape)
+
+
+def swiglu_f32(y, I: int) -> np.ndarray:
+    """y bf16 bits [R, >= 2I] (gate | up) -> h float32 [R, I] = SiLU(gate) * up in fp32 steps."""
+    y = _c(y, np.uint16)
+    R, ldy = y.shape
+    h = np.empty((R, I), np.float32)
+    lib().orc_swiglu_f32(_p(y), R, I, ldy, _p(h))
+    return h
+
+
+def swiglu_quant_1x128(y, I: int, flags: int = 0):
+    """y bf16 bits [R, >= 2I] -> (q uint8 [R, I], s float32 [I/128, R])."""
+    y = _c(y, np.uint16)
+    R, ldy = y.shape
+    assert I % 128 == 0 and ldy >= 2 * I
+    q = np.empty((R, I), np.uint8)
+    s = np.empty((I // 128, R), np.float32)
+    lib().orc_swiglu_quant_1x128(_p(y), R, I, ldy, _p(q), _p(s), flags)
     return q, s
 
 

@@ -217,6 +217,76 @@ void orc_quant_act_1x128_f32(const float* x, int64_t M, int64_t K, uint8_t* q, f
     }
 }
 
+/* ------------------------------------------------------------------ */
+/* SwiGLU fused with 1x128 quantisation of its output (the MoE         */
+/* down-projection input; p2: that activation's scales are integral    */
+/* powers of 2)                                                         */
+/* ------------------------------------------------------------------ */
+
+/* e^x in fp32 by the published Cody-Waite method: x = n*ln2 + r with
+ * n = rint(x*log2(e)), ln2 split into a high part exact in 17 bits and a low
+ * part (so n*ln2_hi is exact and r keeps its low bits), e^r by its Taylor
+ * polynomial of degree 7 on |r| <= ln2/2 (Horner form, fused multiply-adds),
+ * then one multiply by 2^n.  x > 88 gives +inf and x < -87 gives 0 (the
+ * callers only form 1 + e^x, where both are exact).  Every step is one IEEE
+ * fp32 operation, so the result is a fixed function of x. */
+float orc_exp_cw(float x) {
+    if (x > 88.0f) return INFINITY;
+    if (x < -87.0f) return 0.0f;
+    const float n = rintf(x * 0x1.715476p+0f);            /* log2(e) */
+    float r = fmaf(-n, 0x1.62e4p-1f, x);                    /* ln2, high part */
+    r = fmaf(-n, 0x1.7f7d1cp-20f, r);                       /* ln2, low part */
+    float p = 0x1.a01a02p-13f;                              /* 1/7! */
+    p = fmaf(p, r, 0x1.6c16c2p-10f);                        /* 1/6! */
+    p = fmaf(p, r, 0x1.111112p-7f);                         /* 1/5! */
+    p = fmaf(p, r, 0x1.555556p-5f);                         /* 1/4! */
+    p = fmaf(p, r, 0x1.555556p-3f);                         /* 1/3! */
+    p = fmaf(p, r, 0.5f);
+    p = fmaf(p, r, 1.0f);
+    p = fmaf(p, r, 1.0f);
+    return p * ldexpf(1.0f, (int)n);                        /* 2^n is a normal number here */
+}
+
+/* h = SiLU(g) * u = (g * sigma(g)) * u with sigma(g) = 1 / (1 + e^-g), each
+ * step one fp32 operation. */
+static float swiglu_one(float g, float u) {
+    const float e = orc_exp_cw(-g);
+    const float d = 1.0f + e;
+    const float sig = 1.0f / d;
+    const float a = g * sig;
+    return a * u;
+}
+
+/* y bf16 [R][ldy] holds gate = y[:, 0:I] and up = y[:, I:2I]; h fp32 [R][I]. */
+void orc_swiglu_f32(const uint16_t* y, int64_t R, int64_t I, int64_t ldy, float* h) {
+#pragma omp parallel for schedule(static)
+    for (int64_t r = 0; r < R; ++r)
+        for (int64_t j = 0; j < I; ++j)
+            h[r * I + j] = swiglu_one(bf16_to_float(y[r * ldy + j]), bf16_to_float(y[r * ldy + I + j]));
+}
+
+/* SwiGLU, then the 1x128 tile rule on the fp32 h: q [R][I], s [I/128][R]. */
+void orc_swiglu_quant_1x128(const uint16_t* y, int64_t R, int64_t I, int64_t ldy, uint8_t* q, float* s,
+                            uint32_t flags) {
+    int64_t nkb = I / 128;
+#pragma omp parallel for schedule(static)
+    for (int64_t r = 0; r < R; ++r) {
+        for (int64_t kb = 0; kb < nkb; ++kb) {
+            float h[128];
+            float amax = 0.0f;
+            for (int i = 0; i < 128; ++i) {
+                const int64_t j = kb * 128 + i;
+                h[i] = swiglu_one(bf16_to_float(y[r * ldy + j]), bf16_to_float(y[r * ldy + I + j]));
+                float v = fabsf(h[i]);
+                if (v > amax) amax = v;
+            }
+            float inv;
+            s[kb * R + r] = orc_tile_scale(amax, flags, &inv);
+            for (int i = 0; i < 128; ++i) q[r * I + kb * 128 + i] = quant_one(h[i], inv);
+        }
+    }
+}
+
 /* 128x1 activation tiles along tokens, output transposed:
  * x bf16 [T][ldx] (H used columns), qT [H][T], s [T/128][H]. */
 void orc_quant_act_128x1(const uint16_t* x, int64_t T, int64_t H, int64_t ldx,
