@@ -425,6 +425,8 @@ def measure_rows(F, S, dev, flush, pk):
     qwu, swu = F.fp8_quant_weight_128x128(wst)
     ms = _time(lambda: F.fp8_quant_weight_128x128(wst, qwu, swu), 3, 1, flush, st)
     hbm_row("a3_quant_weight_moe_up", ms, E * Nu * K * 3 + E * (Nu // 128) * (K // 128) * 4, "256 x [4096,7168]")
+    P = F.FP8_SCALE_POW2
+    qwu2, swu2 = F.fp8_quant_weight_128x128(wst, flags=P)
     del wst
     yu = torch.empty((R, Nu), dtype=torch.bfloat16, device=dev)
     ms = _time(lambda: F.fp8_grouped_gemm_blockscaled(qa, sa, qwu, swu, r["off"], d=yu), reps, warm, flush, st)
@@ -433,7 +435,14 @@ def measure_rows(F, S, dev, flush, pk):
     tensor_row("a6_grouped_moe_up", ms, 2.0 * R * Nu * K, "32768 rows, 256 experts, N=4096, K=7168",
                dict(weight_bytes=wbytes, hbm_achieved_gbs=round(moved / (ms * 1e-3) / 1e9, 1),
                     hbm_frac=round(moved / (ms * 1e-3) / 1e9 / pk["hbm"], 4)))
-    del qwu, yu, qa, qx
+    qx2, sx2 = F.fp8_quant_act_1x128(x, flags=P)
+    qa2, sa2 = F.fp8_permute_rows(qx2, sx2, r["src_row"])
+    ms = _time(lambda: F.fp8_grouped_gemm_blockscaled_pow2(qa2, sa2, qwu2, swu2, r["off"], d=yu), reps, warm, flush, st)
+    tensor_row("f1_grouped_moe_up_pow2", ms, 2.0 * R * Nu * K,
+               "32768 rows, 256 experts, N=4096, K=7168, pow-2 scales (microscaled MMA)",
+               dict(weight_bytes=wbytes, hbm_achieved_gbs=round(moved / (ms * 1e-3) / 1e9, 1),
+                    hbm_frac=round(moved / (ms * 1e-3) / 1e9 / pk["hbm"], 4)))
+    del qwu, qwu2, yu, qa, qx, qa2, qx2
 
     # MoE down-proj + combine
     md = S.moe_down(with_weights=False)
@@ -452,6 +461,7 @@ def measure_rows(F, S, dev, flush, pk):
     del yup, qg, sg
     wst = S.expert_weights(1, E, Nd, Kd, device=dev)
     qwd, swd = F.fp8_quant_weight_128x128(wst)
+    qwd2, swd2 = F.fp8_quant_weight_128x128(wst, flags=P)
     del wst
     yd = torch.empty((R, Nd), dtype=torch.bfloat16, device=dev)
     ms = _time(lambda: F.fp8_grouped_gemm_blockscaled(qh, sh, qwd, swd, r["off"], d=yd), reps, warm, flush, st)
@@ -460,6 +470,14 @@ def measure_rows(F, S, dev, flush, pk):
     tensor_row("a6_grouped_moe_down", ms, 2.0 * R * Nd * Kd, "32768 rows, 256 experts, N=7168, K=2048",
                dict(weight_bytes=wbytes, hbm_achieved_gbs=round(moved / (ms * 1e-3) / 1e9, 1),
                     hbm_frac=round(moved / (ms * 1e-3) / 1e9 / pk["hbm"], 4)))
+    qh2, sh2 = F.fp8_quant_act_1x128(h, flags=P)
+    yd2 = torch.empty((R, Nd), dtype=torch.bfloat16, device=dev)
+    ms = _time(lambda: F.fp8_grouped_gemm_blockscaled_pow2(qh2, sh2, qwd2, swd2, r["off"], d=yd2), reps, warm, flush, st)
+    tensor_row("f1_grouped_moe_down_pow2", ms, 2.0 * R * Nd * Kd,
+               "32768 rows, 256 experts, N=7168, K=2048, pow-2 scales (microscaled MMA)",
+               dict(weight_bytes=wbytes, hbm_achieved_gbs=round(moved / (ms * 1e-3) / 1e9, 1),
+                    hbm_frac=round(moved / (ms * 1e-3) / 1e9 / pk["hbm"], 4)))
+    del qwd2, qh2, yd2
     outc = torch.empty((Tn, Nd), dtype=torch.bfloat16, device=dev)
     ms = _time(lambda: F.fp8_moe_combine_bf16(yd, r["pos"], r["gate"], out=outc), reps, warm, flush, st)
     hbm_row("a7_combine_bf16", ms, R * Nd * 2 + Tn * Nd * 2 + R * 8, "[32768,7168] bf16 -> [4096,7168]")

@@ -44,6 +44,7 @@
 // and lets the CTA drain its copies in flight, release its tensor memory and
 // exit (both CTAs meet at a final cluster barrier first).
 #include "common.cuh"
+#include "expert_sched.cuh"
 #include "tensor_map.cuh"
 
 namespace fp8bs {
@@ -58,7 +59,6 @@ constexpr int kThreads = 384;           // 12 warps = 3 warpgroups
 constexpr int kPromoThreads = 256;      // warps 4..11
 constexpr int kPromoWarps = kPromoThreads / 32;
 constexpr int kTmemCols = 512;
-constexpr int kMaxExperts = 1024;
 // Scales travel in the pipeline stage through rank-1 TMA maps.  A tensor
 // copy starts on a 16-byte boundary of global memory, so the sA box
 // (kSaBox floats) starts at the tile's first row rounded down to a multiple
@@ -163,8 +163,7 @@ struct DensePairSched {
     }
 };
 
-// Grouped pair tiles: expert e has ceil(ceil(rows_e / 128) / 2) row-tile
-// pairs; per expert, its column tiles x row pairs with the row pair innermost.
+// Grouped pair tiles: the per-expert list of expert_sched.cuh.
 struct GroupedPairSched {
     const int32_t* off_s;
     const int32_t* pre_s;    // prefix of row-pair counts [E+1]
@@ -172,19 +171,12 @@ struct GroupedPairSched {
     int64_t num_n;
     FP8_DEV int64_t count() const { return int64_t(pre_s[E]) * num_n; }
     FP8_DEV Tile get(int64_t w) const {
-        int lo = 0, hi = E;
-        while (hi - lo > 1) {
-            const int mid = (lo + hi) >> 1;
-            if (int64_t(pre_s[mid]) * num_n <= w) lo = mid; else hi = mid;
-        }
-        const int e = lo;
-        const int64_t mt2 = pre_s[e + 1] - pre_s[e];
-        const int64_t local = w - int64_t(pre_s[e]) * num_n;
+        const ExpertTile x = expert_pair_tile(off_s, pre_s, E, num_n, w);
         Tile t;
-        t.e = e;
-        t.n0 = int32_t(local / mt2);
-        t.row0 = int64_t(off_s[e]) + (local % mt2) * (2 * BM);
-        t.row_end = off_s[e + 1];
+        t.e = x.e;
+        t.n0 = int32_t(x.col_tile);
+        t.row0 = x.row0;
+        t.row_end = x.row_end;
         return t;
     }
 };
@@ -245,33 +237,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         int32_t* off_s = reinterpret_cast<int32_t*>(smem + L::kGrpOff);
         int32_t* pre_s = off_s + (kMaxExperts + 1);
         const int E = args.E;
-        bool bad = false;
-        for (int i = threadIdx.x; i <= E; i += kThreads) off_s[i] = __ldg(args.off + i);
-        __syncthreads();
-        if (warp == 0) {
-            int carry = 0;
-            if (lane == 0) pre_s[0] = 0;
-            for (int base = 0; base < E; base += 32) {
-                const int e = base + lane;
-                int cnt = 0;
-                if (e < E) {
-                    const int64_t lo = off_s[e], hi = off_s[e + 1];
-                    const bool ok = lo >= 0 && lo <= hi && hi <= args.M;
-                    bad |= !ok;
-                    cnt = ok ? int(((hi - lo + BM - 1) / BM + 1) / 2) : 0;
-                }
-                int incl = cnt;
-#pragma unroll
-                for (int o = 1; o < 32; o <<= 1) {
-                    const int v = __shfl_up_sync(0xFFFFFFFFu, incl, o);
-                    if (lane >= o) incl += v;
-                }
-                if (e < E) pre_s[e + 1] = carry + incl;
-                carry += __shfl_sync(0xFFFFFFFFu, incl, 31);
-            }
-            bad |= (lane == 0) && (off_s[0] != 0 || int64_t(off_s[E]) != args.M);
-            if (__any_sync(0xFFFFFFFFu, bad) && lane == 0 && blockIdx.x == 0) record_status(FP8_ERR_OFFSETS);
-        }
+        if (expert_pair_prefix(args.off, E, args.M, off_s, pre_s) && threadIdx.x == 0 && blockIdx.x == 0)
+            record_status(FP8_ERR_OFFSETS);
         gs = GroupedPairSched{off_s, pre_s, E, (args.N + BN - 1) / BN};
     } else {
         ds = DensePairSched{(args.M + 2 * BM - 1) / (2 * BM), (args.N + BN - 1) / BN, args.M};

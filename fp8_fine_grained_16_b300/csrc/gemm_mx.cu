@@ -48,6 +48,7 @@
 // Every wait is bounded (2 s); an expired wait records FP8_ERR_TIMEOUT, raises
 // the CTA's abort flag, and the CTA drains and leaves as in the other GEMM.
 #include "common.cuh"
+#include "expert_sched.cuh"
 #include "tensor_map.cuh"
 
 namespace fp8bs {
@@ -77,10 +78,12 @@ struct Args {
     const float* sa;
     const float* sb;
     void* d;
-    int64_t M, N, K;
+    int64_t M, N, K;         // grouped: M = total rows of all experts
+    const int32_t* off;      // grouped only: expert offsets [E+1]
+    int E;                   // grouped only
 };
 
-template <int STAGES>
+template <int STAGES, bool GROUPED>
 struct Layout {
     static constexpr int kABytes = BM * BK;                     // 16 KB
     static constexpr int kBBytes = (BN / 2) * BK;               // 14 KB
@@ -90,17 +93,19 @@ struct Layout {
     static constexpr int kBarOff = kXchgOff + 2 * 8 * 32 * 4;
     static constexpr int kNumBars = 2 * STAGES + 2 + 2 + 2 + 2 + 1;
     static constexpr int kMiscOff = kBarOff + kNumBars * 8;
-    static constexpr int kBytes = kMiscOff + 16;
+    static constexpr int kGrpOff = kMiscOff + 16;                // grouped: offsets and row-pair prefix
+    static constexpr int kGrpBytes = GROUPED ? 2 * (kMaxExperts + 1) * 4 : 0;
+    static constexpr int kBytes = kGrpOff + kGrpBytes;
     static constexpr int kDynSmem = kBytes + 1024;
     static_assert(kABytes % 1024 == 0 && kBBytes % 1024 == 0, "operand tiles on 1024-byte boundaries");
     static_assert(kDynSmem <= 232448, "shared memory per CTA");
 };
 
-template <int STAGES, int BMODE, bool OUT_F32>
+template <int STAGES, int BMODE, bool OUT_F32, bool GROUPED>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_mx_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                         const Args args) {
-    using L = Layout<STAGES>;
+    using L = Layout<STAGES, GROUPED>;
     constexpr uint32_t kIdesc = idesc_mx_e4m3(2 * BM, BN);
 
     extern __shared__ uint8_t smem_raw[];
@@ -122,7 +127,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const bool leader = rank == 0;
     const int64_t nkb = args.K / BK;
     const int64_t num_m2 = (args.M + 2 * BM - 1) / (2 * BM);
-    const int64_t num_tiles = num_m2 * ((args.N + BN - 1) / BN);
+    const int64_t num_n = (args.N + BN - 1) / BN;
     const int64_t cluster = blockIdx.x >> 1, nclusters = gridDim.x >> 1;
 
     if (threadIdx.x == 0) {
@@ -148,14 +153,43 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_alloc_pair(tmem_base_s, kTmemCols);
         tmem_relinquish_pair();
     }
+    // grouped: the per-expert tile list (offsets and row-pair prefix in shared memory)
+    int32_t* off_s = reinterpret_cast<int32_t*>(smem + L::kGrpOff);
+    int32_t* pre_s = off_s + (kMaxExperts + 1);
+    int64_t num_tiles = num_m2 * num_n;
+    if constexpr (GROUPED) {
+        if (expert_pair_prefix(args.off, args.E, args.M, off_s, pre_s) && threadIdx.x == 0 && blockIdx.x == 0)
+            mx_record(FP8_ERR_OFFSETS);
+        num_tiles = int64_t(pre_s[args.E]) * num_n;
+    }
     tc_fence_before();
     cluster_sync();
     tc_fence_after();
     const uint32_t tmem_base = *tmem_base_s;
 
-    // tile w: row pair w % num_m2, column tile w / num_m2; this CTA's rows start at row0
-    auto tile_row0 = [&](int64_t w) { return (w % num_m2) * (2 * BM) + int64_t(rank) * BM; };
-    auto tile_n0 = [&](int64_t w) { return (w / num_m2) * BN; };
+    // Tile w.  Dense: row pair w % num_m2, column tile w / num_m2.  Grouped:
+    // the expert list.  row0 is this CTA's first row; rows >= row_end are
+    // computed but not stored.
+    struct TileAt {
+        int64_t row0, row_end, n0;
+        int e;
+    };
+    auto tile_at = [&](int64_t w) {
+        TileAt t;
+        if constexpr (GROUPED) {
+            const ExpertTile x = expert_pair_tile(off_s, pre_s, args.E, num_n, w);
+            t.row0 = x.row0 + int64_t(rank) * BM;
+            t.row_end = x.row_end;
+            t.n0 = x.col_tile * BN;
+            t.e = x.e;
+        } else {
+            t.row0 = (w % num_m2) * (2 * BM) + int64_t(rank) * BM;
+            t.row_end = args.M;
+            t.n0 = (w / num_m2) * BN;
+            t.e = 0;
+        }
+        return t;
+    };
     // K blocks this cluster walks in all (every tile has nkb)
     const int64_t my_tiles = cluster < num_tiles ? (num_tiles - 1 - cluster) / nclusters + 1 : 0;
     const int64_t my_iters = my_tiles * nkb;
@@ -167,15 +201,19 @@ __global__ void __launch_bounds__(kThreads, 1)
             uint32_t it = 0;
             bool ok = true;
             for (int64_t w = cluster; ok && w < num_tiles; w += nclusters) {
-                const int64_t row0 = tile_row0(w), n0 = tile_n0(w);
+                const TileAt t = tile_at(w);
                 for (int64_t kb = 0; kb < nkb; ++kb) {
                     const uint32_t stage = it % STAGES, phase = (it / STAGES) & 1u;
                     if (!mbar_wait_bounded(&empty[stage], phase ^ 1u, abort_s)) { ok = false; break; }
                     uint8_t* st = smem + stage * L::kStageBytes;
                     const uint32_t fbar = full0 + stage * 8;
                     if (leader) mbar_arrive_expect_tx(&full[stage], L::kPairTxBytes);
-                    tma_load_2d_pair(st, &tmA, fbar, int32_t(kb * BK), int32_t(row0));
-                    tma_load_2d_pair(st + L::kABytes, &tmB, fbar, int32_t(kb * BK), int32_t(n0 + rank * (BN / 2)));
+                    tma_load_2d_pair(st, &tmA, fbar, int32_t(kb * BK), int32_t(t.row0));
+                    if constexpr (GROUPED)
+                        tma_load_3d_pair(st + L::kABytes, &tmB, fbar, int32_t(kb * BK), int32_t(t.n0 + rank * (BN / 2)),
+                                         t.e);
+                    else
+                        tma_load_2d_pair(st + L::kABytes, &tmB, fbar, int32_t(kb * BK), int32_t(t.n0 + rank * (BN / 2)));
                     ++it;
                 }
             }
@@ -263,19 +301,22 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t t_lane = uint32_t(32 * q) << 16;
         const uint32_t sff0 = mapa_shared(&sff[0], 0);
         const int nblk = int(args.N / 128);
-        const uint32_t unkb = uint32_t(nkb), um2 = uint32_t(num_m2);
+        const uint32_t unkb = uint32_t(nkb);
         // Position of a K block in this cluster's walk, advanced one K block at
         // a time (tile coordinates change once per tile: no per-K-block division).
         struct Pos {
             uint32_t kb, w;
             int64_t m;          // this thread's row
             int32_t n0;         // first column of the tile
+            int64_t sb0;        // grouped: the expert's first B-scale row block (e * N/128)
         };
         auto set_tile = [&](Pos& p) {
-            p.m = int64_t(p.w % um2) * (2 * BM) + int64_t(rank) * BM + r;
-            p.n0 = int32_t(p.w / um2) * BN;
+            const TileAt t = tile_at(p.w);
+            p.m = t.row0 + r;
+            p.n0 = int32_t(t.n0);
+            p.sb0 = int64_t(t.e) * nblk;
         };
-        Pos pl{0, uint32_t(cluster), 0, 0};
+        Pos pl{0, uint32_t(cluster), 0, 0, 0};
         set_tile(pl);
         // The four scale warps share the B scales: warp q loads and packs tile
         // column groups j = q and q + 4 (columns 32j + lane) and passes the
@@ -295,7 +336,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const int n = pl.n0 + 32 * j + lane;
                     float v = 1.0f;
                     if (live && j < kBCols && n < args.N) {
-                        if constexpr (BMODE == 0) v = __ldg(args.sb + int64_t(min(n >> 7, nblk - 1)) * nkb + pl.kb);
+                        if constexpr (BMODE == 0)
+                            v = __ldg(args.sb + (pl.sb0 + min(n >> 7, nblk - 1)) * nkb + pl.kb);
                         else v = __ldg(args.sb + int64_t(pl.kb) * args.N + n);
                     }
                     ub[b][jj] = __float_as_uint(v);
@@ -378,7 +420,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         bool ok = true;
         for (int64_t w = cluster; ok && w < num_tiles; w += nclusters, ++tc) {
             const uint32_t buf = tc & 1u;
-            const int64_t m = tile_row0(w) + r, n0 = tile_n0(w);
+            const TileAt t = tile_at(w);
+            const int64_t m = t.row0 + r, n0 = t.n0;
             bool got = true;
             if (lane == 0) got = mbar_wait_bounded(&accf[buf], (tc >> 1) & 1u, abort_s);
             got = __shfl_sync(0xFFFFFFFFu, got ? 1 : 0, 0) != 0;
@@ -391,7 +434,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tmem_ld_32x32b_x32(tcol + 32 * c, v);
                 tmem_wait_ld_regs(v);
                 const int64_t n = n0 + 32 * c;
-                if (m < args.M && n < args.N) {
+                if (m < t.row_end && m < args.M && n < args.N) {
                     if constexpr (OUT_F32) {
                         float4* dst = reinterpret_cast<float4*>(reinterpret_cast<float*>(args.d) + m * args.N + n);
 #pragma unroll
@@ -428,10 +471,10 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 constexpr int kStages = 7;
 
-template <int BMODE, bool OUT_F32>
+template <int BMODE, bool OUT_F32, bool GROUPED>
 static int launch(const CUtensorMap& ma, const CUtensorMap& mb, const Args& args, int sms, cudaStream_t stream) {
-    using Lay = Layout<kStages>;
-    auto kern = gemm_mx_pair_kernel<kStages, BMODE, OUT_F32>;
+    using Lay = Layout<kStages, GROUPED>;
+    auto kern = gemm_mx_pair_kernel<kStages, BMODE, OUT_F32, GROUPED>;
     static bool attr_set = false;
     if (!attr_set) {
         if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Lay::kDynSmem) != cudaSuccess)
@@ -479,17 +522,45 @@ extern "C" int fp8_gemm_blockscaled_pow2(const uint8_t* a, const float* sa, cons
     CUtensorMap ma, mb;
     if (!make_operand_map(&ma, a, M, K, mx::BM, 1, false) || !make_operand_map(&mb, b, N, K, mx::BN / 2, 1, false))
         return FP8_ERR_CUDA;
-    const mx::Args args{sa, sb, d, M, N, K};
+    const mx::Args args{sa, sb, d, M, N, K, nullptr, 0};
     const int64_t pair_tiles = ((M + 2 * mx::BM - 1) / (2 * mx::BM)) * ((N + mx::BN - 1) / mx::BN);
     if (pair_tiles * (K / 128) >= (int64_t(1) << 31) || N + mx::BN >= (int64_t(1) << 31)) return FP8_ERR_SHAPE;
     const int grid_sms = int(2 * pair_tiles < sms ? 2 * pair_tiles : sms);
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     if (b_scale_mode == FP8_BSCALE_BLOCK128) {
-        if (d_dtype == FP8_OUT_BF16) return mx::launch<0, false>(ma, mb, args, grid_sms, s);
-        return mx::launch<0, true>(ma, mb, args, grid_sms, s);
+        if (d_dtype == FP8_OUT_BF16) return mx::launch<0, false, false>(ma, mb, args, grid_sms, s);
+        return mx::launch<0, true, false>(ma, mb, args, grid_sms, s);
     }
-    if (d_dtype == FP8_OUT_BF16) return mx::launch<1, false>(ma, mb, args, grid_sms, s);
-    return mx::launch<1, true>(ma, mb, args, grid_sms, s);
+    if (d_dtype == FP8_OUT_BF16) return mx::launch<1, false, false>(ma, mb, args, grid_sms, s);
+    return mx::launch<1, true, false>(ma, mb, args, grid_sms, s);
+}
+
+extern "C" int fp8_grouped_gemm_blockscaled_pow2(const uint8_t* a, const float* sa, const uint8_t* b, const float* sb,
+                                                 const int32_t* expert_offsets, int E, int64_t total_rows, int64_t N,
+                                                 int64_t K, uint16_t* d, fp8_stream_t stream) {
+    if (!b || !sb || !expert_offsets || E <= 0 || E > kMaxExperts || total_rows < 0 || N <= 0 || K <= 0)
+        return FP8_ERR_ARG;
+    if (K % 128 || N % 128) return FP8_ERR_SHAPE;
+    if (total_rows > (int64_t(1) << 31) - 1 || N > (int64_t(1) << 31) - 1 || K > (int64_t(1) << 31) - 1)
+        return FP8_ERR_SHAPE;
+    if (total_rows == 0) return FP8_OK;
+    if (!a || !sa || !d) return FP8_ERR_ARG;
+    if (!aligned16(a) || !aligned16(b) || !aligned16(d) || !aligned16(sa) || !aligned16(sb) ||
+        (reinterpret_cast<uintptr_t>(expert_offsets) & 3u))
+        return FP8_ERR_ALIGN;
+    // at most total_rows/256 + E row pairs, each with ceil(N/224) column tiles of K/128 blocks
+    const int64_t max_tiles = (total_rows / (2 * mx::BM) + E) * ((N + mx::BN - 1) / mx::BN);
+    if (max_tiles * (K / 128) >= (int64_t(1) << 31) || int64_t(E) * (N / 128) * (K / 128) >= (int64_t(1) << 31) ||
+        N + mx::BN >= (int64_t(1) << 31))
+        return FP8_ERR_SHAPE;
+    const int sms = device_sms();
+    if (sms <= 0) return FP8_ERR_DEVICE;
+    CUtensorMap ma, mb;
+    if (!make_operand_map(&ma, a, total_rows, K, mx::BM, 1, false) ||
+        !make_operand_map(&mb, b, N, K, mx::BN / 2, E, true))
+        return FP8_ERR_CUDA;
+    const mx::Args args{sa, sb, d, total_rows, N, K, expert_offsets, E};
+    return mx::launch<0, false, true>(ma, mb, args, sms, reinterpret_cast<cudaStream_t>(stream));
 }
 
 // Status word of this translation unit: read and clear (synchronising).

@@ -14,39 +14,56 @@
 // library expf, so h is a fixed function of (g, u) and the codes can be
 // checked bit for bit.  That e^x is within 1 ulp of the exact value.
 //
-// One warp per row; each half-warp quantises one 128-column tile (16 lanes x
-// 8 values, 16-byte loads of gate and up), its amax reduced with shuffles.
+// One warp per row; each half-warp quantises 128-column tiles (16 lanes x 8
+// values, 16-byte loads of gate and up; two tiles' loads in flight), the
+// amax reduced with shuffles.  Pairs of elements go through two-lane packed
+// fp32 operations, lane by lane the same IEEE operations.
 #include "common.cuh"
 
 namespace fp8bs {
 
-// e^x for the fp32 SwiGLU above.  x > 88 gives +inf and x < -87 gives 0:
-// only 1 + e^x is formed, where both are exact.
-FP8_DEV float exp_cody_waite(float x) {
-    if (x > 88.0f) return __int_as_float(0x7F800000);
-    if (x < -87.0f) return 0.0f;
-    const float n = rintf(__fmul_rn(x, 0x1.715476p+0f));     // x * log2(e), to the nearest integer
-    float r = __fmaf_rn(-n, 0x1.62e4p-1f, x);                 // ln2, high part (n * it is exact)
-    r = __fmaf_rn(-n, 0x1.7f7d1cp-20f, r);                    // ln2, low part
-    float p = 0x1.a01a02p-13f;                                // 1/7!
-    p = __fmaf_rn(p, r, 0x1.6c16c2p-10f);                     // 1/6!
-    p = __fmaf_rn(p, r, 0x1.111112p-7f);                      // 1/5!
-    p = __fmaf_rn(p, r, 0x1.555556p-5f);                      // 1/4!
-    p = __fmaf_rn(p, r, 0x1.555556p-3f);                      // 1/3!
-    p = __fmaf_rn(p, r, 0.5f);
-    p = __fmaf_rn(p, r, 1.0f);
-    p = __fmaf_rn(p, r, 1.0f);
-    return __fmul_rn(p, __int_as_float((int(n) + 127) << 23));   // 2^n, n in [-126, 127]
+// e^x of two values for the fp32 SwiGLU above, with two-lane packed fp32
+// operations (each lane is the same IEEE operation as its scalar form).
+// x > 88 gives +inf and x < -87 gives 0: only 1 + e^x is formed, where both
+// are exact.  In-range inputs take the steps unchanged; out-of-range ones are
+// clamped for the arithmetic and replaced at the end.
+FP8_DEV float2 exp2_cody_waite(float2 x) {
+    const float2 xc = make_float2(fminf(fmaxf(x.x, -87.0f), 88.0f), fminf(fmaxf(x.y, -87.0f), 88.0f));
+    const float2 t = __fmul2_rn(xc, make_float2(0x1.715476p+0f, 0x1.715476p+0f));   // x * log2(e)
+    // t to the nearest integer (ties to even, as rint): adding 1.5 * 2^23 leaves
+    // the rounded integer in the low mantissa bits of the sum (|t| < 128), and
+    // subtracting it again gives n exactly -- full-rate adds instead of
+    // float -> integer conversions.
+    const float2 big = __fadd2_rn(t, make_float2(0x1.8p23f, 0x1.8p23f));
+    const float2 n = __fadd2_rn(big, make_float2(-0x1.8p23f, -0x1.8p23f));
+    const int nx = __float_as_int(big.x) - 0x4B400000, ny = __float_as_int(big.y) - 0x4B400000;
+    const float2 mn = make_float2(-n.x, -n.y);
+    float2 r = __ffma2_rn(mn, make_float2(0x1.62e4p-1f, 0x1.62e4p-1f), xc);        // ln2, high part (exact product)
+    r = __ffma2_rn(mn, make_float2(0x1.7f7d1cp-20f, 0x1.7f7d1cp-20f), r);          // ln2, low part
+    float2 p = make_float2(0x1.a01a02p-13f, 0x1.a01a02p-13f);                      // 1/7!
+    p = __ffma2_rn(p, r, make_float2(0x1.6c16c2p-10f, 0x1.6c16c2p-10f));            // 1/6!
+    p = __ffma2_rn(p, r, make_float2(0x1.111112p-7f, 0x1.111112p-7f));              // 1/5!
+    p = __ffma2_rn(p, r, make_float2(0x1.555556p-5f, 0x1.555556p-5f));              // 1/4!
+    p = __ffma2_rn(p, r, make_float2(0x1.555556p-3f, 0x1.555556p-3f));              // 1/3!
+    p = __ffma2_rn(p, r, make_float2(0.5f, 0.5f));
+    p = __ffma2_rn(p, r, make_float2(1.0f, 1.0f));
+    p = __ffma2_rn(p, r, make_float2(1.0f, 1.0f));
+    const float2 e = __fmul2_rn(p, make_float2(__int_as_float((nx + 127) << 23),       // 2^n, n in [-126, 127]
+                                                __int_as_float((ny + 127) << 23)));
+    const float inf = __int_as_float(0x7F800000);
+    return make_float2(x.x > 88.0f ? inf : (x.x < -87.0f ? 0.0f : e.x), x.y > 88.0f ? inf : (x.y < -87.0f ? 0.0f : e.y));
 }
 
-// (g * sigma(g)) * u with sigma(g) = 1 / (1 + e^-g); the reciprocal is the
-// correctly rounded one, equal to the IEEE quotient 1 / (1 + e^-g).
-FP8_DEV float swiglu_fp32(float g, float u) {
-    const float sig = __frcp_rn(__fadd_rn(1.0f, exp_cody_waite(-g)));
-    return __fmul_rn(__fmul_rn(g, sig), u);
+// (g * sigma(g)) * u for two elements, sigma(g) = 1 / (1 + e^-g); the
+// reciprocal is the correctly rounded one, equal to the IEEE quotient.
+FP8_DEV float2 swiglu2_fp32(float2 g, float2 u) {
+    const float2 d = __fadd2_rn(make_float2(1.0f, 1.0f), exp2_cody_waite(make_float2(-g.x, -g.y)));
+    const float2 sig = make_float2(__frcp_rn(d.x), __frcp_rn(d.y));
+    return __fmul2_rn(__fmul2_rn(g, sig), u);
 }
 
 constexpr int kSgRows = 8;          // rows (warps) per CTA
+constexpr int kSgTiles = 2;         // tiles per half-warp per iteration (loads in flight)
 
 template <bool POW2>
 __global__ void __launch_bounds__(256) swiglu_quant_1x128_kernel(const uint16_t* __restrict__ y, int64_t R, int64_t I,
@@ -58,37 +75,50 @@ __global__ void __launch_bounds__(256) swiglu_quant_1x128_kernel(const uint16_t*
     const int half = lane >> 4, l16 = lane & 15;
     const int ntiles = int(I >> 7);
     const uint16_t* yr = y + row * ldy;
-    for (int t0 = 0; t0 < ntiles; t0 += 2) {
-        const int tile = t0 + half;
-        const bool live = tile < ntiles;                     // an odd last tile leaves half-warp 1 idle
-        const int64_t col = int64_t(tile) * 128 + l16 * 8;
-        float h[8];
-        float amax = 0.0f;
-        if (live) {
-            const uint4 gv = __ldg(reinterpret_cast<const uint4*>(yr + col));
-            const uint4 uv = __ldg(reinterpret_cast<const uint4*>(yr + I + col));
-            const uint32_t gw[4] = {gv.x, gv.y, gv.z, gv.w}, uw[4] = {uv.x, uv.y, uv.z, uv.w};
+    for (int t0 = 0; t0 < ntiles; t0 += 2 * kSgTiles) {
+        // half-warp `half` takes tiles t0 + half + 2u, u < kSgTiles
+        uint4 gv[kSgTiles], uv[kSgTiles];
 #pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                h[2 * j] = swiglu_fp32(bf16_lo(gw[j]), bf16_lo(uw[j]));
-                h[2 * j + 1] = swiglu_fp32(bf16_hi(gw[j]), bf16_hi(uw[j]));
+        for (int u = 0; u < kSgTiles; ++u) {
+            const int tile = t0 + half + 2 * u;
+            if (tile < ntiles) {
+                const int64_t col = int64_t(tile) * 128 + l16 * 8;
+                gv[u] = __ldg(reinterpret_cast<const uint4*>(yr + col));
+                uv[u] = __ldg(reinterpret_cast<const uint4*>(yr + I + col));
             }
-#pragma unroll
-            for (int i = 0; i < 8; ++i) amax = fmaxf(amax, fabsf(h[i]));
         }
-        // amax of the tile: xor offsets below 16 stay inside the half-warp
 #pragma unroll
-        for (int o = 8; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, o));
-        if (live) {
-            float inv;
-            const float sc = tile_scale(amax, POW2, inv);
-            uint2 o;
-            o.x = cvt_e4m3x2(__fmul_rn(h[0], inv), __fmul_rn(h[1], inv)) |
-                  (cvt_e4m3x2(__fmul_rn(h[2], inv), __fmul_rn(h[3], inv)) << 16);
-            o.y = cvt_e4m3x2(__fmul_rn(h[4], inv), __fmul_rn(h[5], inv)) |
-                  (cvt_e4m3x2(__fmul_rn(h[6], inv), __fmul_rn(h[7], inv)) << 16);
-            *reinterpret_cast<uint2*>(q + row * I + col) = o;
-            if (l16 == 0) s[int64_t(tile) * R + row] = sc;
+        for (int u = 0; u < kSgTiles; ++u) {
+            const int tile = t0 + half + 2 * u;
+            const bool live = tile < ntiles;                 // the last tiles may leave a half-warp idle
+            float2 h[4];
+            float amax = 0.0f;
+            if (live) {
+                const uint32_t gw[4] = {gv[u].x, gv[u].y, gv[u].z, gv[u].w};
+                const uint32_t uw[4] = {uv[u].x, uv[u].y, uv[u].z, uv[u].w};
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    h[j] = swiglu2_fp32(make_float2(bf16_lo(gw[j]), bf16_hi(gw[j])),
+                                        make_float2(bf16_lo(uw[j]), bf16_hi(uw[j])));
+                    amax = fmaxf(amax, fmaxf(fabsf(h[j].x), fabsf(h[j].y)));
+                }
+            }
+            // amax of the tile: xor offsets below 16 stay inside the half-warp
+#pragma unroll
+            for (int o = 8; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, o));
+            if (live) {
+                float inv;
+                const float sc = tile_scale(amax, POW2, inv);
+                const float2 inv2 = make_float2(inv, inv);
+                float2 c[4];
+#pragma unroll
+                for (int j = 0; j < 4; ++j) c[j] = __fmul2_rn(h[j], inv2);
+                uint2 o;
+                o.x = cvt_e4m3x2(c[0].x, c[0].y) | (cvt_e4m3x2(c[1].x, c[1].y) << 16);
+                o.y = cvt_e4m3x2(c[2].x, c[2].y) | (cvt_e4m3x2(c[3].x, c[3].y) << 16);
+                *reinterpret_cast<uint2*>(q + row * I + int64_t(tile) * 128 + l16 * 8) = o;
+                if (l16 == 0) s[int64_t(tile) * R + row] = sc;
+            }
         }
     }
 }

@@ -52,6 +52,7 @@ _SIGS = {
     "fp8_swiglu_quant_1x128": [_P, _I64, _I64, _I64, _P, _P, _U32, _P],
     "fp8_transpose_128x128": [_P, _P, _I64, _I64, _P, _P, _P],
     "fp8_grouped_gemm_blockscaled": [_P, _P, _P, _P, _P, _I, _I64, _I64, _I64, _P, _P],
+    "fp8_grouped_gemm_blockscaled_pow2": [_P, _P, _P, _P, _P, _I, _I64, _I64, _I64, _P, _P],
     "fp8_moe_route_topk": [_P, _I64, _I, _I, _P, _P, _P, _P, _P, _P, _P],
     "fp8_moe_route_topk_noalloc": [_P, _I64, _I, _I, _P, _P, _P, _P, _P, _P],
     "fp8_permute_rows": [_P, _P, _I64, _I64, _P, _I64, _P, _P, _P],
@@ -235,6 +236,21 @@ def fp8_transpose_128x128(q, s, qT=None, sT=None, stream=None):
         _ptr(q, torch.uint8, "q"), _ptr(s, torch.float32, "s"), N, K, _ptr(qT, torch.uint8, "qT"),
         _ptr(sT, torch.float32, "sT"), _stream(stream)))
     return qT, sT
+
+
+def fp8_grouped_gemm_blockscaled_pow2(a, sa, b, sb, expert_offsets, d=None, stream=None) -> torch.Tensor:
+    """As fp8_grouped_gemm_blockscaled, for power-of-two scales applied by the tensor core."""
+    R, K = a.shape
+    E, N, Kb = b.shape
+    if Kb != K:
+        raise ValueError("a and b disagree on K")
+    if d is None:
+        d = torch.empty((R, N), dtype=torch.bfloat16, device=b.device)
+    _check("fp8_grouped_gemm_blockscaled_pow2", lib.fp8_grouped_gemm_blockscaled_pow2(
+        _ptr(a, torch.uint8, "a"), _ptr(sa, torch.float32, "sa"), _ptr(b, torch.uint8, "b"),
+        _ptr(sb, torch.float32, "sb"), _ptr(expert_offsets, torch.int32, "expert_offsets"), E, R, N, K,
+        _ptr(d, torch.bfloat16, "d"), _stream(stream)))
+    return d
 
 
 def fp8_grouped_gemm_blockscaled(a, sa, b, sb, expert_offsets, d=None, stream=None) -> torch.Tensor:

@@ -211,6 +211,21 @@ FP8_API int fp8_gemm_blockscaled_pow2(const uint8_t* a, const float* sa,
                                       fp8_stream_t stream);
 
 /* ------------------------------------------------------------------------
+ * The grouped (per-expert) GEMM for power-of-two scales, on the microscaled
+ * MMA of fp8_gemm_blockscaled_pow2 (page 4: 256 routed experts, each
+ * processing the rows dispatched to it; pages 2/3: power-of-two scales,
+ * tensor cores that take the scaling factors).  Arguments, layouts, limits
+ * and the handling of bad offsets are those of fp8_grouped_gemm_blockscaled;
+ * every scale read must be a positive normal power of two (FP8_ERR_SCALE in
+ * the device status otherwise).
+ * ---------------------------------------------------------------------- */
+FP8_API int fp8_grouped_gemm_blockscaled_pow2(const uint8_t* a, const float* sa,
+                                              const uint8_t* b, const float* sb,
+                                              const int32_t* expert_offsets, int E,
+                                              int64_t total_rows, int64_t N, int64_t K,
+                                              uint16_t* d, fp8_stream_t stream);
+
+/* ------------------------------------------------------------------------
  * Transposed copy of a 128x128-block-quantised E4M3 matrix, for FP8 Dgrad
  * (page 1: E4M3 on all tensors, Dgrad included; page 4: weights quantised
  * per 128x128 block).  The amax of a 128x128 block is the same after
