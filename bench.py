@@ -277,7 +277,12 @@ def run_ours(args, ws, rank, local):
             e2e_ms.append(e_start.elapsed_time(e_end))
     e2e = sum(e2e_ms) / len(e2e_ms)
 
-    rows = measure_rows(F, S, dev, flush, pk) if args.rows == "all" else None
+    if args.rows == "all":
+        rows = measure_rows(F, S, dev, flush, pk)
+    elif args.rows == "none":
+        rows = None
+    else:
+        rows = measure_rows(F, S, dev, flush, pk, tuple(x for x in args.rows.split(",") if x))
 
     out = {
         "metric": METRIC,
@@ -330,8 +335,12 @@ def _time(fn, reps, warm, flush, stream):
     return statistics.median(ts)
 
 
-def measure_rows(F, S, dev, flush, pk):
-    """Each step of the path on its own workload, median of timed reps."""
+ROW_SECTIONS = ("dense", "wgrad", "moe_up", "moe_down", "swiglu")
+
+
+def measure_rows(F, S, dev, flush, pk, sections=ROW_SECTIONS):
+    """Each step of the path on its own workload, median of timed reps.
+    `sections` picks which groups of rows run (each builds its own inputs)."""
     st = torch.cuda.current_stream()
     reps, warm = 20, 3
     fp8_peak = pk["bf16"] * 2.0
@@ -352,7 +361,23 @@ def measure_rows(F, S, dev, flush, pk):
             r.update(extra)
         out[name] = r
 
-    # dense linear rows
+    if "dense" in sections:
+        measure_dense_rows(F, S, dev, flush, st, reps, warm, hbm_row, tensor_row, out)
+    if "wgrad" in sections:
+        measure_wgrad_rows(F, S, dev, flush, st, reps, warm, hbm_row, tensor_row, out)
+    if "moe_up" in sections:
+        measure_moe_up_rows(F, S, dev, flush, st, reps, warm, hbm_row, tensor_row, out, pk)
+    if "moe_down" in sections:
+        measure_moe_down_rows(F, S, dev, flush, st, reps, warm, hbm_row, tensor_row, out, pk)
+    if "swiglu" in sections:
+        measure_swiglu_rows(F, dev, flush, st, reps, warm, hbm_row)
+    torch.cuda.synchronize()
+    if F.fp8_get_status() != 0:
+        raise RuntimeError("device status set while timing rows")
+    return out
+
+
+def measure_dense_rows(F, S, dev, flush, st, reps, warm, hbm_row, tensor_row, out):
     d = S.dense_linear()
     x, w = d["x"].to(dev), d["w"].to(dev)
     qx, sx = F.fp8_quant_act_1x128(x)
@@ -387,7 +412,8 @@ def measure_rows(F, S, dev, flush, pk):
     tensor_row("f1_gemm_dense_pow2", ms, GEMM_FLOP, "4096x7168x7168 -> bf16, pow-2 scales as UE8M0 (microscaled MMA)")
     del x, w, qx, qw, y, qwT, dy, qdy, qx2, qw2
 
-    # Wgrad rows
+
+def measure_wgrad_rows(F, S, dev, flush, st, reps, warm, hbm_row, tensor_row, out):
     d = S.wgrad()
     T, H = d["dy"].shape
     dy, xx = d["dy"].to(dev), d["x"].to(dev)
@@ -407,8 +433,9 @@ def measure_rows(F, S, dev, flush, pk):
     tensor_row("f1_gemm_wgrad_pow2", ms, 2.0 * H * H * T, "dW = dY^T X, 7168x7168x8192 -> fp32, pow-2 scales")
     del dy, xx, qa, qb, dw, qa2, qb2
 
-    # MoE up-proj
-    E, k = 256, 8
+
+def measure_moe_up_rows(F, S, dev, flush, st, reps, warm, hbm_row, tensor_row, out, pk):
+    E, k, K = 256, 8, 7168
     mu = S.moe_up(with_weights=False)
     x, logits = mu["x"].to(dev), mu["logits"].to(dev)
     Tn = x.shape[0]
@@ -444,21 +471,18 @@ def measure_rows(F, S, dev, flush, pk):
                     hbm_frac=round(moved / (ms * 1e-3) / 1e9 / pk["hbm"], 4)))
     del qwu, qwu2, yu, qa, qx, qa2, qx2
 
-    # MoE down-proj + combine
+
+def measure_moe_down_rows(F, S, dev, flush, st, reps, warm, hbm_row, tensor_row, out, pk):
+    E, k, P = 256, 8, F.FP8_SCALE_POW2
     md = S.moe_down(with_weights=False)
     h, logits = md["h"].to(dev), md["logits"].to(dev)
     r = F.fp8_moe_route_topk(logits, k)
     Kd, Nd = 2048, 7168
+    Tn = logits.shape[0]
+    R = Tn * k
     qh, sh = F.fp8_quant_act_1x128(h)
     ms = _time(lambda: F.fp8_quant_act_1x128(h, qh, sh), reps, warm, flush, st)
     hbm_row("a1_quant_act_1x128_moe_down", ms, R * Kd * 3 + R * (Kd // 128) * 4, "h [32768,2048]")
-    # the same input formed from the up-projection output: SwiGLU fused with power-of-two 1x128 quantisation
-    yup = torch.randn((R, 2 * Kd), generator=torch.Generator(device=dev).manual_seed(5), device=dev).to(torch.bfloat16)
-    qg, sg = F.fp8_swiglu_quant_1x128(yup, Kd)
-    ms = _time(lambda: F.fp8_swiglu_quant_1x128(yup, Kd, qg, sg), reps, warm, flush, st)
-    hbm_row("f4_swiglu_quant_1x128_pow2", ms, R * 2 * Kd * 2 + R * Kd + R * (Kd // 128) * 4,
-            "[32768, 2 x 2048] bf16 -> h = SiLU(gate)*up as E4M3 + pow-2 scales")
-    del yup, qg, sg
     wst = S.expert_weights(1, E, Nd, Kd, device=dev)
     qwd, swd = F.fp8_quant_weight_128x128(wst)
     qwd2, swd2 = F.fp8_quant_weight_128x128(wst, flags=P)
@@ -481,10 +505,18 @@ def measure_rows(F, S, dev, flush, pk):
     outc = torch.empty((Tn, Nd), dtype=torch.bfloat16, device=dev)
     ms = _time(lambda: F.fp8_moe_combine_bf16(yd, r["pos"], r["gate"], out=outc), reps, warm, flush, st)
     hbm_row("a7_combine_bf16", ms, R * Nd * 2 + Tn * Nd * 2 + R * 8, "[32768,7168] bf16 -> [4096,7168]")
-    torch.cuda.synchronize()
-    if F.fp8_get_status() != 0:
-        raise RuntimeError("device status set while timing rows")
-    return out
+
+
+def measure_swiglu_rows(F, dev, flush, st, reps, warm, hbm_row):
+    """The MoE down-projection input formed from the up-projection output
+    (32768 dispatched rows, gate | up of 2 x 2048): SwiGLU fused with
+    power-of-two 1x128 quantisation."""
+    R, Kd = 32768, 2048
+    yup = torch.randn((R, 2 * Kd), generator=torch.Generator(device=dev).manual_seed(5), device=dev).to(torch.bfloat16)
+    qg, sg = F.fp8_swiglu_quant_1x128(yup, Kd)
+    ms = _time(lambda: F.fp8_swiglu_quant_1x128(yup, Kd, qg, sg), reps, warm, flush, st)
+    hbm_row("f4_swiglu_quant_1x128_pow2", ms, R * 2 * Kd * 2 + R * Kd + R * (Kd // 128) * 4,
+            "[32768, 2 x 2048] bf16 -> h = SiLU(gate)*up as E4M3 + pow-2 scales")
 
 
 # ---------------------------------------------------------------- oracle (CPU) arm
@@ -543,7 +575,8 @@ def main():
     ap.add_argument("--steps", type=int, default=1000)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--rows", choices=["all", "none"], default="all")
+    ap.add_argument("--rows", default="all",
+                    help="all | none | comma-separated sections of %s" % ",".join(ROW_SECTIONS))
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()
     if args.warmup < 3:
