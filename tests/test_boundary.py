@@ -102,3 +102,37 @@ def test_moe_argument_errors(fb):
     assert L.fp8_permute_rows(None, None, 10, 128, None, 0, None, None, None) == 0
     assert L.fp8_moe_combine_bf16(FAKE, 10, FAKE, FAKE, 4, 2, 12, FAKE, None) == -2
     assert L.fp8_selftest_wait_timeout(0, None) == -1
+
+
+def test_pow2_and_fused_entry_point_argument_errors(fb):
+    L = fb.lib
+    # power-of-two GEMM: the argument rules of fp8_gemm_blockscaled
+    p = L.fp8_gemm_blockscaled_pow2
+    assert p(None, FAKE, FAKE, FAKE, 0, FAKE, 0, 128, 256, 256, None) == -1                  # null a
+    assert p(FAKE, FAKE, FAKE, FAKE, 3, FAKE, 0, 128, 256, 256, None) == -1                  # B-scale mode
+    assert p(FAKE, FAKE, FAKE, FAKE, 0, FAKE, 0, 128, 200, 256, None) == -2                  # N % 128
+    assert p(FAKE, FAKE, FAKE, FAKE, 0, FAKE + 4, 0, 128, 256, 256, None) == -3              # misaligned d
+    gp = L.fp8_grouped_gemm_blockscaled_pow2
+    assert gp(FAKE, FAKE, FAKE, FAKE, FAKE, 0, 10, 256, 256, FAKE, None) == -1               # E = 0
+    assert gp(FAKE, FAKE, FAKE, FAKE, FAKE, 4, 10, 256, 200, FAKE, None) == -2               # K % 128
+    assert gp(None, None, FAKE, FAKE, FAKE, 4, 0, 256, 256, None, None) == 0                 # no rows: no-op
+    # quantised epilogue
+    q = L.fp8_gemm_blockscaled_q8
+    assert q(FAKE, FAKE, FAKE, FAKE, 0, None, FAKE, 0, 128, 256, 256, None) == -1            # null q_out
+    assert q(FAKE, FAKE, FAKE, FAKE, 0, FAKE, FAKE, 4, 128, 256, 256, None) == -1            # unknown flag
+    assert q(FAKE, FAKE, FAKE, FAKE, 0, FAKE, FAKE, 0, 128, 256, 100, None) == -2            # K % 128
+    assert q(FAKE, FAKE, FAKE, FAKE, 0, FAKE + 8, FAKE, 0, 128, 256, 256, None) == -3        # misaligned q_out
+    assert q(FAKE, FAKE, FAKE, FAKE, 0, FAKE, FAKE + 2, 0, 128, 256, 256, None) == -3        # misaligned s_out
+    # SwiGLU + quantisation
+    s = L.fp8_swiglu_quant_1x128
+    assert s(FAKE, 4, 128, 255, FAKE, FAKE, 1, None) == -1                                   # ldy < 2I
+    assert s(FAKE, 4, 100, 200, FAKE, FAKE, 1, None) == -2                                   # I % 128
+    assert s(FAKE, 4, 128, 260, FAKE, FAKE, 1, None) == -3                                   # ldy % 8
+    assert s(FAKE, 0, 128, 256, FAKE, FAKE, 1, None) == -1                                   # R = 0
+    assert s(FAKE, 4, 128, 256, FAKE, FAKE, 2, None) == -1                                   # unknown flag
+    # transposed copy for Dgrad
+    t = L.fp8_transpose_128x128
+    assert t(FAKE, FAKE, 100, 128, FAKE, FAKE, None) == -2                                   # N % 128
+    assert t(FAKE + 4, FAKE, 128, 128, FAKE, FAKE, None) == -3                               # misaligned q
+    assert t(None, FAKE, 128, 128, FAKE, FAKE, None) == -1
+    assert "power of two" in fb.fp8_strerror(fb.FP8_ERR_SCALE)
