@@ -104,22 +104,6 @@ FP8_DEV bool mbar_test_wait(uint64_t* bar, uint32_t parity) {
     return ok != 0;
 }
 
-// Probe two barriers at once: both tests are in flight together, so the
-// pair costs about one probe.  True when both phases have completed.
-FP8_DEV bool mbar_test_wait2(uint64_t* b0, uint32_t p0, uint64_t* b1, uint32_t p1) {
-    uint32_t ok;
-    asm volatile(
-        "{\n\t.reg .pred a, b;\n\t"
-        "mbarrier.test_wait.parity.shared::cta.b64 a, [%1], %2;\n\t"
-        "mbarrier.test_wait.parity.shared::cta.b64 b, [%3], %4;\n\t"
-        "and.pred a, a, b;\n\t"
-        "selp.u32 %0, 1, 0, a;\n\t}"
-        : "=r"(ok)
-        : "r"(smem_u32(b0)), "r"(p0), "r"(smem_u32(b1)), "r"(p1)
-        : "memory");
-    return ok != 0;
-}
-
 // Wait for the phase of `bar` with the given parity, giving up after
 // timeout_ns or as soon as *abort becomes non-zero.  On a timeout the waiter
 // raises *abort itself.  Returns true when the phase completed.  A phase that
@@ -152,48 +136,12 @@ FP8_DEV void tma_load_1d(void* dst, const CUtensorMap* map, uint64_t* bar, int32
         "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(c0)
         : "memory");
 }
-FP8_DEV void tma_load_2d(void* dst, const CUtensorMap* map, uint64_t* bar, int32_t c0, int32_t c1) {
-    asm volatile(
-        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%3, %4}], [%2];" ::"r"(
-            smem_u32(dst)),
-        "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(c0), "r"(c1)
-        : "memory");
-}
-FP8_DEV void tma_load_3d(void* dst, const CUtensorMap* map, uint64_t* bar, int32_t c0, int32_t c1, int32_t c2) {
-    asm volatile(
-        "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%3, %4, %5}], [%2];" ::"r"(
-            smem_u32(dst)),
-        "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(c0), "r"(c1), "r"(c2)
-        : "memory");
-}
 
 // ---------------------------------------------------------------- tcgen05
-FP8_DEV void tmem_alloc(uint32_t* dst_smem, uint32_t ncols) {
-    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(dst_smem)),
-                 "r"(ncols)
-                 : "memory");
-}
-FP8_DEV void tmem_relinquish() { asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory"); }
-FP8_DEV void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
-    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
-}
+// Ordering of tcgen05 operations around thread synchronisation (barriers,
+// mbarrier waits) between the threads that issue and observe them.
 FP8_DEV void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
 FP8_DEV void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
-
-// D(tmem) (+)= A(smem) * B(smem)^T, E4M3 x E4M3 -> F32, one CTA.
-FP8_DEV void umma_e4m3(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc, uint32_t accumulate) {
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "setp.ne.b32 p, %4, 0;\n\t"
-        "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
-        : "memory");
-}
-// Arrive once on `bar` when every tcgen05 op issued so far by this thread is done.
-FP8_DEV void umma_commit(uint64_t* bar) {
-    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_u32(bar))
-                 : "memory");
-}
 
 // ---------------------------------------------------------------- CTA pairs
 // A cluster of two CTAs on neighbouring SMs drives one tcgen05 MMA of M=256
@@ -353,7 +301,6 @@ FP8_DEV void tmem_ld_32x32b_x32(uint32_t taddr, uint32_t (&v)[32]) {
         : "r"(taddr)
         : "memory");
 }
-FP8_DEV void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 // 32 lanes x 64 consecutive 32-bit columns into one register array.
 FP8_DEV void tmem_ld_32x32b_x64(uint32_t taddr, uint32_t (&v)[64]) {
     asm volatile(
@@ -387,18 +334,6 @@ FP8_DEV void tmem_wait_ld_regs64(uint32_t (&v)[64]) {
           "+r"(v[56]), "+r"(v[57]), "+r"(v[58]), "+r"(v[59]), "+r"(v[60]), "+r"(v[61]), "+r"(v[62]), "+r"(v[63])
         :
         : "memory");
-}
-
-// Compiler-only fence: the registers in v are treated as modified here, so
-// their uses cannot move above this point (placed right after a
-// tcgen05.wait::ld that covers the load that wrote them).
-FP8_DEV void regs_fence(uint32_t (&v)[32]) {
-    asm volatile(""
-                 : "+r"(v[0]), "+r"(v[1]), "+r"(v[2]), "+r"(v[3]), "+r"(v[4]), "+r"(v[5]), "+r"(v[6]), "+r"(v[7]),
-                   "+r"(v[8]), "+r"(v[9]), "+r"(v[10]), "+r"(v[11]), "+r"(v[12]), "+r"(v[13]), "+r"(v[14]),
-                   "+r"(v[15]), "+r"(v[16]), "+r"(v[17]), "+r"(v[18]), "+r"(v[19]), "+r"(v[20]), "+r"(v[21]),
-                   "+r"(v[22]), "+r"(v[23]), "+r"(v[24]), "+r"(v[25]), "+r"(v[26]), "+r"(v[27]), "+r"(v[28]),
-                   "+r"(v[29]), "+r"(v[30]), "+r"(v[31]));
 }
 
 // tcgen05.wait::ld that also names the registers a preceding tcgen05.ld
