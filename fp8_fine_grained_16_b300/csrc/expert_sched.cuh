@@ -1,11 +1,12 @@
 // expert_sched.cuh -- per-expert tile lists of the grouped (MoE) GEMMs.
 //
 // Expert e owns rows [off[e], off[e+1]) of A and D (page 4: each token's
-// rows are dispatched to its routed experts).  A CTA pair covers 256 rows,
-// so expert e needs ceil(ceil(rows_e / 128) / 2) row pairs, each crossed with
-// every column tile of the output.  Tiles are numbered expert by expert, and
-// within an expert column tile by column tile with the row pairs innermost,
-// so the pairs that stream one weight tile run next to each other.
+// rows are dispatched to its routed experts).  A tile covers tile_rows rows
+// (256 for a CTA pair, 128 for one CTA), so expert e needs
+// ceil(rows_e / tile_rows) row tiles, each crossed with every column tile of
+// the output.  Tiles are numbered expert by expert, and within an expert
+// column tile by column tile with the row tiles innermost, so the tiles that
+// stream one weight tile run next to each other.
 #pragma once
 #include "common.cuh"
 
@@ -13,13 +14,14 @@ namespace fp8bs {
 
 constexpr int kMaxExperts = 1024;
 
-// Offsets into shared memory and the exclusive prefix of row-pair counts,
-// pre_s[e] = row pairs of the experts before e (pre_s[E] = all).  Every
+// Offsets into shared memory and the exclusive prefix of row-tile counts,
+// pre_s[e] = row tiles of the experts before e (pre_s[E] = all).  Every
 // thread of the CTA calls it (it synchronises the CTA twice).  An expert
 // whose offsets are not 0 <= off[e] <= off[e+1] <= total_rows gets no rows;
 // the result is true in every thread when any offset breaks the rules,
 // including off[0] != 0 or off[E] != total_rows.
-FP8_DEV bool expert_pair_prefix(const int32_t* off, int E, int64_t total_rows, int32_t* off_s, int32_t* pre_s) {
+FP8_DEV bool expert_tile_prefix(const int32_t* off, int E, int64_t total_rows, int32_t* off_s, int32_t* pre_s,
+                                int tile_rows) {
     __shared__ int bad_s;
     for (int i = threadIdx.x; i <= E; i += blockDim.x) off_s[i] = __ldg(off + i);
     if (threadIdx.x == 0) bad_s = 0;
@@ -36,7 +38,7 @@ FP8_DEV bool expert_pair_prefix(const int32_t* off, int E, int64_t total_rows, i
                 const int64_t lo = off_s[e], hi = off_s[e + 1];
                 const bool ok = lo >= 0 && lo <= hi && hi <= total_rows;
                 bad |= !ok;
-                cnt = ok ? int(((hi - lo + 127) / 128 + 1) / 2) : 0;
+                cnt = ok ? int((hi - lo + tile_rows - 1) / tile_rows) : 0;
             }
             int incl = cnt;
 #pragma unroll
@@ -55,14 +57,15 @@ FP8_DEV bool expert_pair_prefix(const int32_t* off, int E, int64_t total_rows, i
 }
 
 struct ExpertTile {
-    int64_t row0;            // first row of the pair (global row index)
+    int64_t row0;            // first row of the tile (global row index)
     int64_t row_end;         // rows >= row_end belong to the next expert: not stored
     int64_t col_tile;        // column tile index
     int e;                   // expert
 };
 
-// Tile w of the list above (num_n column tiles per row pair).
-FP8_DEV ExpertTile expert_pair_tile(const int32_t* off_s, const int32_t* pre_s, int E, int64_t num_n, int64_t w) {
+// Tile w of the list above (num_n column tiles per row tile).
+FP8_DEV ExpertTile expert_tile(const int32_t* off_s, const int32_t* pre_s, int E, int64_t num_n, int64_t w,
+                               int tile_rows) {
     int lo = 0, hi = E;
     while (hi - lo > 1) {
         const int mid = (lo + hi) >> 1;
@@ -73,7 +76,7 @@ FP8_DEV ExpertTile expert_pair_tile(const int32_t* off_s, const int32_t* pre_s, 
     ExpertTile t;
     t.e = lo;
     t.col_tile = local / mt2;
-    t.row0 = int64_t(off_s[lo]) + (local % mt2) * 256;
+    t.row0 = int64_t(off_s[lo]) + (local % mt2) * tile_rows;
     t.row_end = off_s[lo + 1];
     return t;
 }

@@ -117,6 +117,7 @@ struct Tile {
 //                        MMA commit of that K block (its accumulator is ready).
 //   empty[s] (each)    = MMA commit + this CTA's 8 promotion warps.
 constexpr int kPairStages = 6;
+constexpr int kSingleStages = 4;     // one CTA holds all 256 B rows: 48 KB of operands per stage
 // Register split (launched with 168 per thread, 64512 in all): warpgroup 0
 // keeps 64 (the producer's per-K-block state spills at 40), the promotion
 // warpgroups get 216 (128 accumulators + one 32-column TMEM batch +
@@ -125,15 +126,15 @@ constexpr int kPairStages = 6;
 constexpr int kPairRegsWG0 = 64, kPairRegsPromo = 216;
 static_assert(128 * kPairRegsWG0 + 256 * kPairRegsPromo <= kThreads * 168, "register split");
 
-template <int BN, int STAGES, int BMODE, bool GROUPED>
+template <bool PAIR, int BN, int STAGES, int BMODE, bool GROUPED>
 struct PairLayout {
     static constexpr int kABytes = BM * BK;                      // this CTA's 128 rows
-    static constexpr int kBBytes = (BN / 2) * BK;                // this CTA's half of B
+    static constexpr int kBBytes = (PAIR ? BN / 2 : BN) * BK;    // this CTA's half of B (all of it alone)
     static constexpr int kSaOff = kABytes + kBBytes;
     static constexpr int kSbOff = kSaOff + kSaRegion;
     static constexpr int kSbRegion = BMODE == 1 ? BN * 4 : 2 * kSbHalf0 * 4;
     static constexpr int kStageBytes = (kSbOff + kSbRegion + 1023) & ~1023;
-    static constexpr uint32_t kPairTxBytes = 2 * (kABytes + kBBytes);   // leader's full[s]: both CTAs
+    static constexpr uint32_t kPairTxBytes = (PAIR ? 2 : 1) * (kABytes + kBBytes);   // leader's full[s]: both CTAs
     static constexpr uint32_t kScaleTxBytes = kSaBox * 4 + (BMODE == 1 ? BN * 4 : 2 * kSbBox0 * 4);
     static constexpr int kStagesBytes = STAGES * kStageBytes;
     static constexpr int kBarOff = kStagesBytes;  // full[S], sfull[S], empty[S], done
@@ -149,13 +150,15 @@ struct PairLayout {
     static_assert(kDynSmem <= 232448, "shared memory per CTA");
 };
 
-// Dense pair tiles: w -> pair row tile w % num_m2 (256 rows), column tile w / num_m2.
+// Dense tiles of `rows` rows (256 for a CTA pair, 128 for one CTA):
+// w -> row tile w % num_m2, column tile w / num_m2.
 struct DensePairSched {
     int64_t num_m2, num_n, M;
+    int rows;
     FP8_DEV int64_t count() const { return num_m2 * num_n; }
     FP8_DEV Tile get(int64_t w) const {
         Tile t;
-        t.row0 = (w % num_m2) * (2 * BM);
+        t.row0 = (w % num_m2) * rows;
         t.row_end = M;
         t.n0 = int32_t(w / num_m2);
         t.e = 0;
@@ -163,15 +166,16 @@ struct DensePairSched {
     }
 };
 
-// Grouped pair tiles: the per-expert list of expert_sched.cuh.
+// Grouped tiles: the per-expert list of expert_sched.cuh.
 struct GroupedPairSched {
     const int32_t* off_s;
-    const int32_t* pre_s;    // prefix of row-pair counts [E+1]
+    const int32_t* pre_s;    // prefix of row-tile counts [E+1]
     int E;
     int64_t num_n;
+    int rows;
     FP8_DEV int64_t count() const { return int64_t(pre_s[E]) * num_n; }
     FP8_DEV Tile get(int64_t w) const {
-        const ExpertTile x = expert_pair_tile(off_s, pre_s, E, num_n, w);
+        const ExpertTile x = expert_tile(off_s, pre_s, E, num_n, w, rows);
         Tile t;
         t.e = x.e;
         t.n0 = int32_t(x.col_tile);
@@ -181,16 +185,18 @@ struct GroupedPairSched {
     }
 };
 
-template <int BN, int STAGES, int BMODE, int OUT, bool GROUPED>
+template <bool PAIR, int BN, int STAGES, int BMODE, int OUT, bool GROUPED>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                      const __grid_constant__ CUtensorMap tmSA, const __grid_constant__ CUtensorMap tmSB,
                      const GemmArgs args) {
-    using L = PairLayout<BN, STAGES, BMODE, GROUPED>;
+    using L = PairLayout<PAIR, BN, STAGES, BMODE, GROUPED>;
     static_assert(2 * BN <= kTmemCols, "two accumulators must fit in TMEM");
     static_assert(BN == 256, "one promotion half = 128 columns = one scale block and one column per warpgroup thread");
     constexpr int kHalf = BN / 2;
-    constexpr uint32_t kIdesc = idesc_e4m3_f32(2 * BM, BN);     // M = 256 across the pair
+    constexpr int kCtas = PAIR ? 2 : 1;
+    constexpr int kTileRows = kCtas * BM;
+    constexpr uint32_t kIdesc = idesc_e4m3_f32(kTileRows, BN);  // M = 256 across a pair, 128 alone
 
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -204,15 +210,16 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
-    const uint32_t rank = cluster_ctarank();
+    const uint32_t rank = PAIR ? cluster_ctarank() : 0u;
     const bool leader = rank == 0;
     const int64_t nkb = args.K / BK;
-    const int64_t cluster = blockIdx.x >> 1, nclusters = gridDim.x >> 1;
+    // a "cluster" is the pair, or the CTA itself
+    const int64_t cluster = PAIR ? blockIdx.x >> 1 : blockIdx.x, nclusters = PAIR ? gridDim.x >> 1 : gridDim.x;
 
     // ---------------- set-up
     if (threadIdx.x == 0) {
         for (int i = 0; i < STAGES; ++i) {
-            mbar_init(&full[i], 1 + 2 * kPromoWarps);
+            mbar_init(&full[i], 1 + kCtas * kPromoWarps);
             mbar_init(&sfull[i], 2);
             mbar_init(&empty[i], 1 + kPromoWarps);
         }
@@ -227,8 +234,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         tma_prefetch_desc(&tmSB);
     }
     if (warp == 1) {
-        tmem_alloc_pair(tmem_base_s, kTmemCols);
-        tmem_relinquish_pair();
+        if constexpr (PAIR) {
+            tmem_alloc_pair(tmem_base_s, kTmemCols);
+            tmem_relinquish_pair();
+        } else {
+            tmem_alloc(tmem_base_s, kTmemCols);
+            tmem_relinquish();
+        }
     }
 
     GroupedPairSched gs{};
@@ -237,16 +249,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         int32_t* off_s = reinterpret_cast<int32_t*>(smem + L::kGrpOff);
         int32_t* pre_s = off_s + (kMaxExperts + 1);
         const int E = args.E;
-        if (expert_pair_prefix(args.off, E, args.M, off_s, pre_s) && threadIdx.x == 0 && blockIdx.x == 0)
+        if (expert_tile_prefix(args.off, E, args.M, off_s, pre_s, kTileRows) && threadIdx.x == 0 && blockIdx.x == 0)
             record_status(FP8_ERR_OFFSETS);
-        gs = GroupedPairSched{off_s, pre_s, E, (args.N + BN - 1) / BN};
+        gs = GroupedPairSched{off_s, pre_s, E, (args.N + BN - 1) / BN, kTileRows};
     } else {
-        ds = DensePairSched{(args.M + 2 * BM - 1) / (2 * BM), (args.N + BN - 1) / BN, args.M};
+        ds = DensePairSched{(args.M + kTileRows - 1) / kTileRows, (args.N + BN - 1) / BN, args.M, kTileRows};
     }
     tc_fence_before();
     // Both CTAs' barriers are initialised and the TMEM is allocated before
     // either CTA touches the other's shared memory.
-    cluster_sync();
+    if constexpr (PAIR) cluster_sync(); else __syncthreads();
     tc_fence_after();
     const uint32_t tmem_base = *tmem_base_s;
 
@@ -269,7 +281,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (warp == 0) {
             // ================= TMA producer (each CTA)
             if (lane == 0) {
-                const uint32_t full0 = mapa_shared(&full[0], 0);    // leader's full[0], cluster address
+                const uint32_t full0 = PAIR ? mapa_shared(&full[0], 0) : 0u;   // leader's full[0], cluster address
                 uint32_t it = 0;
                 bool ok = true;
                 for (int64_t w = cluster; ok && w < num_tiles; w += nclusters) {
@@ -288,13 +300,21 @@ __global__ void __launch_bounds__(kThreads, 1)
                         uint8_t* st = smem + stage * L::kStageBytes;
                         const uint32_t fbar = full0 + stage * 8;
                         if (leader) mbar_arrive_expect_tx(&full[stage], L::kPairTxBytes);
-                        tma_load_2d_pair(st, &tmA, fbar, int32_t(kb * BK), int32_t(t.row0));
-                        if constexpr (GROUPED)
-                            tma_load_3d_pair(st + L::kABytes, &tmB, fbar, int32_t(kb * BK),
-                                             t.n0 + int32_t(rank) * (BN / 2), t.e);
-                        else
-                            tma_load_2d_pair(st + L::kABytes, &tmB, fbar, int32_t(kb * BK),
-                                             t.n0 + int32_t(rank) * (BN / 2));
+                        if constexpr (PAIR) {
+                            tma_load_2d_pair(st, &tmA, fbar, int32_t(kb * BK), int32_t(t.row0));
+                            if constexpr (GROUPED)
+                                tma_load_3d_pair(st + L::kABytes, &tmB, fbar, int32_t(kb * BK),
+                                                 t.n0 + int32_t(rank) * (BN / 2), t.e);
+                            else
+                                tma_load_2d_pair(st + L::kABytes, &tmB, fbar, int32_t(kb * BK),
+                                                 t.n0 + int32_t(rank) * (BN / 2));
+                        } else {
+                            tma_load_2d(st, &tmA, &full[stage], int32_t(kb * BK), int32_t(t.row0));
+                            if constexpr (GROUPED)
+                                tma_load_3d(st + L::kABytes, &tmB, &full[stage], int32_t(kb * BK), t.n0, t.e);
+                            else
+                                tma_load_2d(st + L::kABytes, &tmB, &full[stage], int32_t(kb * BK), t.n0);
+                        }
                         mbar_arrive_expect_tx(&sfull[stage], L::kScaleTxBytes);
                         tma_load_1d(st + L::kSaOff, &tmSA, &sfull[stage], int32_t((kb * args.M + t.row0) & ~int64_t(3)));
                         if constexpr (BMODE == 0) {
@@ -338,16 +358,25 @@ __global__ void __launch_bounds__(kThreads, 1)
                         const uint64_t bdesc = sw128_kmajor_desc(b_addr);
                         const uint32_t d_tmem = tmem_base + buf * BN;
 #pragma unroll
-                        for (int k = 0; k < BK / 32; ++k)
-                            umma_e4m3_pair(d_tmem, adesc + 2 * k, bdesc + 2 * k, kIdesc, k > 0 ? 1u : 0u);
-                        umma_commit_pair(&empty[stage], 0x3);
-                        umma_commit_pair(&sfull[stage], 0x3);      // accumulator ready, in both CTAs
+                        for (int k = 0; k < BK / 32; ++k) {
+                            if constexpr (PAIR)
+                                umma_e4m3_pair(d_tmem, adesc + 2 * k, bdesc + 2 * k, kIdesc, k > 0 ? 1u : 0u);
+                            else
+                                umma_e4m3(d_tmem, adesc + 2 * k, bdesc + 2 * k, kIdesc, k > 0 ? 1u : 0u);
+                        }
+                        if constexpr (PAIR) {
+                            umma_commit_pair(&empty[stage], 0x3);
+                            umma_commit_pair(&sfull[stage], 0x3);  // accumulator ready, in both CTAs
+                        } else {
+                            umma_commit(&empty[stage]);
+                            umma_commit(&sfull[stage]);
+                        }
                         ++it;
                         ++g;
                     }
                 }
                 if (!ok) record_status(FP8_ERR_TIMEOUT);
-                umma_commit_pair(done, 0x1);
+                if constexpr (PAIR) umma_commit_pair(done, 0x1); else umma_commit(done);
                 int zero = 0;
                 mbar_wait_bounded(done, 0, reinterpret_cast<volatile int*>(&zero));
             }
@@ -360,12 +389,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int half = (warp - 4) >> 2;
         const int r = wq * 32 + lane;
         const uint32_t t_lane = uint32_t(wq * 32) << 16;
-        const uint32_t full0 = mapa_shared(&full[0], 0);       // leader's full[0], cluster address
+        // release on the leader's full[] (the CTA's own alone)
+        const uint32_t full0 = PAIR ? mapa_shared(&full[0], 0) : smem_u32(&full[0]);
+        auto release = [&](uint32_t stage_i) {
+            if constexpr (PAIR) mbar_arrive_cluster(full0 + stage_i * 8); else mbar_arrive(&full[stage_i]);
+        };
         // the two accumulators start out free: release them to K blocks 0 and 1
         __syncwarp();
         if (lane == 0) {
-            mbar_arrive_cluster(full0);
-            mbar_arrive_cluster(full0 + 8);
+            release(0);
+            release(1);
         }
 
         uint32_t g = 0;
@@ -447,7 +480,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 __syncwarp();
                 // all of P_kb is in registers: accumulator `buf` is free for K
                 // block g + 2 (on the leader's full[])
-                if (lane == 0) mbar_arrive_cluster(full0 + ((g + 2) % STAGES) * 8);
+                if (lane == 0) release((g + 2) % STAGES);
                 scale_chunk(2, v);
                 scale_chunk(3, v + 32);
                 if constexpr (BMODE == 1) {
@@ -509,21 +542,21 @@ __global__ void __launch_bounds__(kThreads, 1)
     // other may still use its shared memory or tensor memory
     tc_fence_before();
     __syncthreads();
-    cluster_sync();
+    if constexpr (PAIR) cluster_sync();
     if (warp == 1) {
         tc_fence_after();
-        tmem_dealloc_pair(tmem_base, kTmemCols);
+        if constexpr (PAIR) tmem_dealloc_pair(tmem_base, kTmemCols); else tmem_dealloc(tmem_base, kTmemCols);
     }
 }
 
 // ---------------------------------------------------------------- host side
 constexpr int kBN = 256;
 
-template <int BN, int STAGES, int BMODE, int OUT, bool GROUPED>
+template <bool PAIR, int BN, int STAGES, int BMODE, int OUT, bool GROUPED>
 static int launch_pair(const CUtensorMap& ma, const CUtensorMap& mb, const CUtensorMap& msa, const CUtensorMap& msb,
                        const GemmArgs& args, int sms, cudaStream_t stream) {
-    using L = PairLayout<BN, STAGES, BMODE, GROUPED>;
-    auto kern = gemm_pair_kernel<BN, STAGES, BMODE, OUT, GROUPED>;
+    using L = PairLayout<PAIR, BN, STAGES, BMODE, GROUPED>;
+    auto kern = gemm_pair_kernel<PAIR, BN, STAGES, BMODE, OUT, GROUPED>;
     static bool attr_set = false;
     if (!attr_set) {
         if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kDynSmem) != cudaSuccess)
@@ -539,6 +572,12 @@ static int launch_pair(const CUtensorMap& ma, const CUtensorMap& mb, const CUten
     cfg.blockDim = dim3(kThreads);
     cfg.dynamicSmemBytes = L::kDynSmem;
     cfg.stream = stream;
+    if constexpr (!PAIR) {
+        // one CTA per SM (shared memory and launch bounds allow no more)
+        cfg.gridDim = dim3(sms);
+        if (cudaLaunchKernelEx(&cfg, kern, ma, mb, msa, msb, args) != cudaSuccess) return FP8_ERR_CUDA;
+        return cudaGetLastError() == cudaSuccess ? FP8_OK : FP8_ERR_CUDA;
+    }
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     int max_clusters = 0;
@@ -594,11 +633,11 @@ extern "C" int fp8_gemm_blockscaled(const uint8_t* a, const float* sa, const uin
     const int grid_sms = int(2 * pair_tiles < sms ? 2 * pair_tiles : sms);
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     if (b_scale_mode == FP8_BSCALE_BLOCK128) {
-        if (d_dtype == FP8_OUT_BF16) return launch_pair<kBN, kPairStages, 0, kOutBF16, false>(ma, mb, msa, msb, args, grid_sms, s);
-        return launch_pair<kBN, kPairStages, 0, kOutF32, false>(ma, mb, msa, msb, args, grid_sms, s);
+        if (d_dtype == FP8_OUT_BF16) return launch_pair<true, kBN, kPairStages, 0, kOutBF16, false>(ma, mb, msa, msb, args, grid_sms, s);
+        return launch_pair<true, kBN, kPairStages, 0, kOutF32, false>(ma, mb, msa, msb, args, grid_sms, s);
     }
-    if (d_dtype == FP8_OUT_BF16) return launch_pair<kBN, kPairStages, 1, kOutBF16, false>(ma, mb, msa, msb, args, grid_sms, s);
-    return launch_pair<kBN, kPairStages, 1, kOutF32, false>(ma, mb, msa, msb, args, grid_sms, s);
+    if (d_dtype == FP8_OUT_BF16) return launch_pair<true, kBN, kPairStages, 1, kOutBF16, false>(ma, mb, msa, msb, args, grid_sms, s);
+    return launch_pair<true, kBN, kPairStages, 1, kOutF32, false>(ma, mb, msa, msb, args, grid_sms, s);
 }
 
 extern "C" int fp8_gemm_blockscaled_q8(const uint8_t* a, const float* sa, const uint8_t* b, const float* sb,
@@ -628,8 +667,8 @@ extern "C" int fp8_gemm_blockscaled_q8(const uint8_t* a, const float* sa, const 
     const int grid_sms = int(2 * pair_tiles < sms ? 2 * pair_tiles : sms);
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     if (b_scale_mode == FP8_BSCALE_BLOCK128)
-        return launch_pair<kBN, kPairStages, 0, kOutE4M3, false>(ma, mb, msa, msb, args, grid_sms, s);
-    return launch_pair<kBN, kPairStages, 1, kOutE4M3, false>(ma, mb, msa, msb, args, grid_sms, s);
+        return launch_pair<true, kBN, kPairStages, 0, kOutE4M3, false>(ma, mb, msa, msb, args, grid_sms, s);
+    return launch_pair<true, kBN, kPairStages, 1, kOutE4M3, false>(ma, mb, msa, msb, args, grid_sms, s);
 }
 
 extern "C" int fp8_grouped_gemm_blockscaled(const uint8_t* a, const float* sa, const uint8_t* b, const float* sb,
@@ -650,12 +689,15 @@ extern "C" int fp8_grouped_gemm_blockscaled(const uint8_t* a, const float* sa, c
     const int sms = device_sms();
     if (sms <= 0) return FP8_ERR_DEVICE;
     CUtensorMap ma, mb, msa, msb;
-    if (!make_operand_map(&ma, a, total_rows, K, BM, 1, false) || !make_operand_map(&mb, b, N, K, kBN / 2, E, true) ||
+    if (!make_operand_map(&ma, a, total_rows, K, BM, 1, false) || !make_operand_map(&mb, b, N, K, kBN, E, true) ||
         !make_scale_map(&msa, sa, total_rows * (K / 128), kSaBox) ||
         !make_scale_map(&msb, sb, int64_t(E) * (N / 128) * (K / 128), kSbBox0))
         return FP8_ERR_CUDA;
     GemmArgs args{sa, sb, d, expert_offsets, total_rows, N, K, E, nullptr, 0u};
-    return launch_pair<kBN, kPairStages, 0, kOutBF16, true>(ma, mb, msa, msb, args, sms, reinterpret_cast<cudaStream_t>(stream));
+    // one CTA per tile: experts hold ~128 rows on average, and each CTA streams
+    // its own weight tiles, so twice as many tiles are in flight as with pairs
+    return launch_pair<false, kBN, kSingleStages, 0, kOutBF16, true>(ma, mb, msa, msb, args, sms,
+                                                                    reinterpret_cast<cudaStream_t>(stream));
 }
 
 extern "C" int fp8_selftest_wait_timeout(uint64_t timeout_ns, fp8_stream_t stream) {

@@ -158,7 +158,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     int32_t* pre_s = off_s + (kMaxExperts + 1);
     int64_t num_tiles = num_m2 * num_n;
     if constexpr (GROUPED) {
-        if (expert_pair_prefix(args.off, args.E, args.M, off_s, pre_s) && threadIdx.x == 0 && blockIdx.x == 0)
+        if (expert_tile_prefix(args.off, args.E, args.M, off_s, pre_s, 2 * BM) && threadIdx.x == 0 && blockIdx.x == 0)
             mx_record(FP8_ERR_OFFSETS);
         num_tiles = int64_t(pre_s[args.E]) * num_n;
     }
@@ -177,7 +177,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     auto tile_at = [&](int64_t w) {
         TileAt t;
         if constexpr (GROUPED) {
-            const ExpertTile x = expert_pair_tile(off_s, pre_s, args.E, num_n, w);
+            const ExpertTile x = expert_tile(off_s, pre_s, args.E, num_n, w, 2 * BM);
             t.row0 = x.row0 + int64_t(rank) * BM;
             t.row_end = x.row_end;
             t.n0 = x.col_tile * BN;
