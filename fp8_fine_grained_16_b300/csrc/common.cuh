@@ -264,16 +264,28 @@ FP8_DEV void umma_commit_pair(uint64_t* bar, uint16_t cta_mask) {
 // and in each 32-bit word the byte chosen by the scale-ID fields of idesc.
 // Called by a whole converged warp: one lane, picked by elect.sync, issues
 // the MMA (the operands are warp-uniform, so they stay in uniform registers).
-FP8_DEV void umma_mx_e4m3_pair_elect(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc, uint32_t sfa,
-                                     uint32_t sfb, uint32_t accumulate) {
-    asm volatile(
-        "{\n\t.reg .pred pe, pa;\n\t"
-        "elect.sync _|pe, 0xffffffff;\n\t"
-        "setp.ne.b32 pa, %6, 0;\n\t"
-        "@pe tcgen05.mma.cta_group::2.kind::mxf8f6f4.block_scale.scale_vec::1X [%0], %1, %2, %3, [%4], [%5], pa;\n\t}" ::"r"(
-            d_tmem),
-        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(sfa), "r"(sfb), "r"(accumulate)
-        : "memory");
+// PAIR: cta_group::2 (M = 256 across a CTA pair); otherwise cta_group::1.
+template <bool PAIR>
+FP8_DEV void umma_mx_e4m3_elect(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc, uint32_t sfa,
+                                uint32_t sfb, uint32_t accumulate) {
+    if constexpr (PAIR)
+        asm volatile(
+            "{\n\t.reg .pred pe, pa;\n\t"
+            "elect.sync _|pe, 0xffffffff;\n\t"
+            "setp.ne.b32 pa, %6, 0;\n\t"
+            "@pe tcgen05.mma.cta_group::2.kind::mxf8f6f4.block_scale.scale_vec::1X [%0], %1, %2, %3, [%4], [%5], pa;\n\t}" ::"r"(
+                d_tmem),
+            "l"(adesc), "l"(bdesc), "r"(idesc), "r"(sfa), "r"(sfb), "r"(accumulate)
+            : "memory");
+    else
+        asm volatile(
+            "{\n\t.reg .pred pe, pa;\n\t"
+            "elect.sync _|pe, 0xffffffff;\n\t"
+            "setp.ne.b32 pa, %6, 0;\n\t"
+            "@pe tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale.scale_vec::1X [%0], %1, %2, %3, [%4], [%5], pa;\n\t}" ::"r"(
+                d_tmem),
+            "l"(adesc), "l"(bdesc), "r"(idesc), "r"(sfa), "r"(sfb), "r"(accumulate)
+            : "memory");
 }
 
 // The same MMA (accumulating), issued between a non-blocking probe of one or
@@ -281,24 +293,48 @@ FP8_DEV void umma_mx_e4m3_pair_elect(uint32_t d_tmem, uint64_t adesc, uint64_t b
 // latency overlaps the issue of the MMA (which waits for the tensor core to
 // accept it).  Returns true when every probed phase has completed; with
 // bar1 == 0 only bar0 is probed.  Whole converged warp, as above.
-FP8_DEV bool umma_mx_e4m3_pair_probe_elect(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
-                                           uint32_t sfa, uint32_t sfb, uint32_t bar0, uint32_t par0, uint32_t bar1,
-                                           uint32_t par1) {
+template <bool PAIR>
+FP8_DEV bool umma_mx_e4m3_probe_elect(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc, uint32_t sfa,
+                                      uint32_t sfb, uint32_t bar0, uint32_t par0, uint32_t bar1, uint32_t par1) {
     uint32_t ok;
-    asm volatile(
-        "{\n\t.reg .pred p0, p1, pe;\n\t"
-        "mbarrier.test_wait.parity.shared::cta.b64 p0, [%7], %8;\n\t"
-        "setp.eq.u32 p1, %9, 0;\n\t"
-        "@!p1 mbarrier.test_wait.parity.shared::cta.b64 p1, [%9], %10;\n\t"
-        "elect.sync _|pe, 0xffffffff;\n\t"
-        "@pe tcgen05.mma.cta_group::2.kind::mxf8f6f4.block_scale.scale_vec::1X [%1], %2, %3, %4, [%5], [%6], 1;\n\t"
-        "and.pred p0, p0, p1;\n\t"
-        "selp.u32 %0, 1, 0, p0;\n\t}"
-        : "=r"(ok)
-        : "r"(d_tmem), "l"(adesc), "l"(bdesc), "r"(idesc), "r"(sfa), "r"(sfb), "r"(bar0), "r"(par0), "r"(bar1),
-          "r"(par1)
-        : "memory");
+    if constexpr (PAIR)
+        asm volatile(
+            "{\n\t.reg .pred p0, p1, pe;\n\t"
+            "mbarrier.test_wait.parity.shared::cta.b64 p0, [%7], %8;\n\t"
+            "setp.eq.u32 p1, %9, 0;\n\t"
+            "@!p1 mbarrier.test_wait.parity.shared::cta.b64 p1, [%9], %10;\n\t"
+            "elect.sync _|pe, 0xffffffff;\n\t"
+            "@pe tcgen05.mma.cta_group::2.kind::mxf8f6f4.block_scale.scale_vec::1X [%1], %2, %3, %4, [%5], [%6], 1;\n\t"
+            "and.pred p0, p0, p1;\n\t"
+            "selp.u32 %0, 1, 0, p0;\n\t}"
+            : "=r"(ok)
+            : "r"(d_tmem), "l"(adesc), "l"(bdesc), "r"(idesc), "r"(sfa), "r"(sfb), "r"(bar0), "r"(par0), "r"(bar1),
+              "r"(par1)
+            : "memory");
+    else
+        asm volatile(
+            "{\n\t.reg .pred p0, p1, pe;\n\t"
+            "mbarrier.test_wait.parity.shared::cta.b64 p0, [%7], %8;\n\t"
+            "setp.eq.u32 p1, %9, 0;\n\t"
+            "@!p1 mbarrier.test_wait.parity.shared::cta.b64 p1, [%9], %10;\n\t"
+            "elect.sync _|pe, 0xffffffff;\n\t"
+            "@pe tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale.scale_vec::1X [%1], %2, %3, %4, [%5], [%6], 1;\n\t"
+            "and.pred p0, p0, p1;\n\t"
+            "selp.u32 %0, 1, 0, p0;\n\t}"
+            : "=r"(ok)
+            : "r"(d_tmem), "l"(adesc), "l"(bdesc), "r"(idesc), "r"(sfa), "r"(sfb), "r"(bar0), "r"(par0), "r"(bar1),
+              "r"(par1)
+            : "memory");
     return ok != 0;
+}
+
+// umma_commit issued by one elected lane of a converged warp (one CTA).
+FP8_DEV void umma_commit_elect(uint64_t* bar) {
+    asm volatile(
+        "{\n\t.reg .pred pe;\n\t"
+        "elect.sync _|pe, 0xffffffff;\n\t"
+        "@pe tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n\t}" ::"r"(smem_u32(bar))
+        : "memory");
 }
 
 // umma_commit_pair issued by one elected lane of a converged warp.

@@ -83,12 +83,12 @@ struct Args {
     int E;                   // grouped only
 };
 
-template <int STAGES, bool GROUPED>
+template <bool PAIR, int STAGES, bool GROUPED>
 struct Layout {
     static constexpr int kABytes = BM * BK;                     // 16 KB
-    static constexpr int kBBytes = (BN / 2) * BK;               // 14 KB
+    static constexpr int kBBytes = (PAIR ? BN / 2 : BN) * BK;   // 14 KB of a pair's B tile, 28 KB alone
     static constexpr int kStageBytes = kABytes + kBBytes;
-    static constexpr uint32_t kPairTxBytes = 2 * (kABytes + kBBytes);
+    static constexpr uint32_t kPairTxBytes = (PAIR ? 2 : 1) * (kABytes + kBBytes);
     static constexpr int kXchgOff = STAGES * kStageBytes;       // packed B scale words, 2 x 8 x 32
     static constexpr int kBarOff = kXchgOff + 2 * 8 * 32 * 4;
     static constexpr int kNumBars = 2 * STAGES + 2 + 2 + 2 + 2 + 1;
@@ -101,12 +101,14 @@ struct Layout {
     static_assert(kDynSmem <= 232448, "shared memory per CTA");
 };
 
-template <int STAGES, int BMODE, bool OUT_F32, bool GROUPED>
+template <bool PAIR, int STAGES, int BMODE, bool OUT_F32, bool GROUPED>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_mx_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                         const Args args) {
-    using L = Layout<STAGES, GROUPED>;
-    constexpr uint32_t kIdesc = idesc_mx_e4m3(2 * BM, BN);
+    using L = Layout<PAIR, STAGES, GROUPED>;
+    constexpr int kCtas = PAIR ? 2 : 1;
+    constexpr int kTileRows = kCtas * BM;
+    constexpr uint32_t kIdesc = idesc_mx_e4m3(kTileRows, BN);
 
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -123,12 +125,13 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
-    const uint32_t rank = cluster_ctarank();
+    const uint32_t rank = PAIR ? cluster_ctarank() : 0u;
     const bool leader = rank == 0;
     const int64_t nkb = args.K / BK;
-    const int64_t num_m2 = (args.M + 2 * BM - 1) / (2 * BM);
+    const int64_t num_m2 = (args.M + kTileRows - 1) / kTileRows;
     const int64_t num_n = (args.N + BN - 1) / BN;
-    const int64_t cluster = blockIdx.x >> 1, nclusters = gridDim.x >> 1;
+    // a "cluster" is the pair, or the CTA itself
+    const int64_t cluster = PAIR ? blockIdx.x >> 1 : blockIdx.x, nclusters = PAIR ? gridDim.x >> 1 : gridDim.x;
 
     if (threadIdx.x == 0) {
         for (int i = 0; i < STAGES; ++i) {
@@ -136,10 +139,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(&empty[i], 1);
         }
         for (int j = 0; j < 2; ++j) {
-            mbar_init(&sff[j], 8);
+            mbar_init(&sff[j], 4 * kCtas);
             mbar_init(&sfe[j], 1);
             mbar_init(&accf[j], 1);
-            mbar_init(&acce[j], 8);
+            mbar_init(&acce[j], 4 * kCtas);
         }
         mbar_init(done, 1);
         *abort_s = 0;
@@ -150,20 +153,25 @@ __global__ void __launch_bounds__(kThreads, 1)
         tma_prefetch_desc(&tmB);
     }
     if (warp == 1) {
-        tmem_alloc_pair(tmem_base_s, kTmemCols);
-        tmem_relinquish_pair();
+        if constexpr (PAIR) {
+            tmem_alloc_pair(tmem_base_s, kTmemCols);
+            tmem_relinquish_pair();
+        } else {
+            tmem_alloc(tmem_base_s, kTmemCols);
+            tmem_relinquish();
+        }
     }
     // grouped: the per-expert tile list (offsets and row-pair prefix in shared memory)
     int32_t* off_s = reinterpret_cast<int32_t*>(smem + L::kGrpOff);
     int32_t* pre_s = off_s + (kMaxExperts + 1);
     int64_t num_tiles = num_m2 * num_n;
     if constexpr (GROUPED) {
-        if (expert_tile_prefix(args.off, args.E, args.M, off_s, pre_s, 2 * BM) && threadIdx.x == 0 && blockIdx.x == 0)
+        if (expert_tile_prefix(args.off, args.E, args.M, off_s, pre_s, kTileRows) && threadIdx.x == 0 && blockIdx.x == 0)
             mx_record(FP8_ERR_OFFSETS);
         num_tiles = int64_t(pre_s[args.E]) * num_n;
     }
     tc_fence_before();
-    cluster_sync();
+    if constexpr (PAIR) cluster_sync(); else __syncthreads();
     tc_fence_after();
     const uint32_t tmem_base = *tmem_base_s;
 
@@ -177,13 +185,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     auto tile_at = [&](int64_t w) {
         TileAt t;
         if constexpr (GROUPED) {
-            const ExpertTile x = expert_tile(off_s, pre_s, args.E, num_n, w, 2 * BM);
+            const ExpertTile x = expert_tile(off_s, pre_s, args.E, num_n, w, kTileRows);
             t.row0 = x.row0 + int64_t(rank) * BM;
             t.row_end = x.row_end;
             t.n0 = x.col_tile * BN;
             t.e = x.e;
         } else {
-            t.row0 = (w % num_m2) * (2 * BM) + int64_t(rank) * BM;
+            t.row0 = (w % num_m2) * kTileRows + int64_t(rank) * BM;
             t.row_end = args.M;
             t.n0 = (w / num_m2) * BN;
             t.e = 0;
@@ -197,7 +205,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (warp == 0) {
         // ================= TMA producer (each CTA)
         if (lane == 0) {
-            const uint32_t full0 = mapa_shared(&full[0], 0);
+            const uint32_t full0 = PAIR ? mapa_shared(&full[0], 0) : 0u;
             uint32_t it = 0;
             bool ok = true;
             for (int64_t w = cluster; ok && w < num_tiles; w += nclusters) {
@@ -208,12 +216,21 @@ __global__ void __launch_bounds__(kThreads, 1)
                     uint8_t* st = smem + stage * L::kStageBytes;
                     const uint32_t fbar = full0 + stage * 8;
                     if (leader) mbar_arrive_expect_tx(&full[stage], L::kPairTxBytes);
-                    tma_load_2d_pair(st, &tmA, fbar, int32_t(kb * BK), int32_t(t.row0));
-                    if constexpr (GROUPED)
-                        tma_load_3d_pair(st + L::kABytes, &tmB, fbar, int32_t(kb * BK), int32_t(t.n0 + rank * (BN / 2)),
-                                         t.e);
-                    else
-                        tma_load_2d_pair(st + L::kABytes, &tmB, fbar, int32_t(kb * BK), int32_t(t.n0 + rank * (BN / 2)));
+                    if constexpr (PAIR) {
+                        tma_load_2d_pair(st, &tmA, fbar, int32_t(kb * BK), int32_t(t.row0));
+                        if constexpr (GROUPED)
+                            tma_load_3d_pair(st + L::kABytes, &tmB, fbar, int32_t(kb * BK),
+                                             int32_t(t.n0 + rank * (BN / 2)), t.e);
+                        else
+                            tma_load_2d_pair(st + L::kABytes, &tmB, fbar, int32_t(kb * BK),
+                                             int32_t(t.n0 + rank * (BN / 2)));
+                    } else {
+                        tma_load_2d(st, &tmA, &full[stage], int32_t(kb * BK), int32_t(t.row0));
+                        if constexpr (GROUPED)
+                            tma_load_3d(st + L::kABytes, &tmB, &full[stage], int32_t(kb * BK), int32_t(t.n0), t.e);
+                        else
+                            tma_load_2d(st + L::kABytes, &tmB, &full[stage], int32_t(kb * BK), int32_t(t.n0));
+                    }
                     ++it;
                 }
             }
@@ -234,6 +251,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             uint32_t it = 0, tc = 0;
             bool ok = true;
             bool ready = false;     // barriers of K block `it` already seen complete
+            // commit to a barrier of both CTAs of a pair (or of the CTA alone)
+            auto commit = [&](uint64_t* bar) {
+                if constexpr (PAIR) umma_commit_pair_elect(bar, 0x3); else umma_commit_elect(bar);
+            };
             auto wait_all = [&](uint64_t* bar, uint32_t parity) {
                 bool got = true;
                 if (lane == 0) got = mbar_wait_bounded(bar, parity, abort_s);
@@ -262,7 +283,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const uint32_t idesc = kIdesc | (b << 4) | (b << 29);      // scale byte b of A and B
 #pragma unroll
                     for (int k = 0; k < BK / 32 - 1; ++k)
-                        umma_mx_e4m3_pair_elect(d_tmem, adesc + 2 * k, bdesc + 2 * k, idesc, sf, sf + 8,
+                        umma_mx_e4m3_elect<PAIR>(d_tmem, adesc + 2 * k, bdesc + 2 * k, idesc, sf, sf + 8,
                                                 (kb > 0 || k > 0) ? 1u : 0u);
                     // The last MMA goes out together with a probe of the next K
                     // block's barriers: the probe's latency overlaps the issue of
@@ -270,21 +291,21 @@ __global__ void __launch_bounds__(kThreads, 1)
                     {
                         const uint32_t nit = it + 1, ns = nit % STAGES, np = (nit / STAGES) & 1u;
                         const uint32_t ng = nit / kGroup;
-                        ready = umma_mx_e4m3_pair_probe_elect(
+                        ready = umma_mx_e4m3_probe_elect<PAIR>(
                             d_tmem, adesc + 2 * (BK / 32 - 1), bdesc + 2 * (BK / 32 - 1), idesc, sf, sf + 8,
                             smem_u32(&full[ns]), np, nit % kGroup == 0 ? smem_u32(&sff[ng & 1u]) : 0u, (ng >> 1) & 1u);
                         ready = __all_sync(0xFFFFFFFFu, ready);
                     }
-                    umma_commit_pair_elect(&empty[stage], 0x3);
-                    if (b == kGroup - 1) umma_commit_pair_elect(&sfe[g & 1u], 0x3);
+                    commit(&empty[stage]);
+                    if (b == kGroup - 1) commit(&sfe[g & 1u]);
                     ++it;
                 }
                 if (!ok) break;
-                umma_commit_pair_elect(&accf[buf], 0x3);
+                commit(&accf[buf]);
             }
             if (!ok && lane == 0) mx_record(FP8_ERR_TIMEOUT);
             // commits track the issuing thread's MMAs: the same elected lane
-            umma_commit_pair_elect(done, 0x1);
+            if constexpr (PAIR) umma_commit_pair_elect(done, 0x1); else umma_commit_elect(done);
             if (lane == 0) {
                 int zero = 0;
                 mbar_wait_bounded(done, 0, reinterpret_cast<volatile int*>(&zero));
@@ -299,7 +320,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int q = warp & 3;
         const int r = 32 * q + lane;
         const uint32_t t_lane = uint32_t(32 * q) << 16;
-        const uint32_t sff0 = mapa_shared(&sff[0], 0);
+        const uint32_t sff0 = PAIR ? mapa_shared(&sff[0], 0) : 0u;
         const int nblk = int(args.N / 128);
         const uint32_t unkb = uint32_t(nkb);
         // Position of a K block in this cluster's walk, advanced one K block at
@@ -404,7 +425,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tmem_wait_st();
                 tc_fence_before();
                 __syncwarp();
-                if (lane == 0) mbar_arrive_cluster(sff0 + (g & 1u) * 8);
+                if (lane == 0) {
+                    if constexpr (PAIR) mbar_arrive_cluster(sff0 + (g & 1u) * 8); else mbar_arrive(&sff[g & 1u]);
+                }
             }
         }
         const bool bad = chk_max >= 0x7F000000u || chk_mant != 0;
@@ -415,7 +438,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int q = warp & 3;
         const int r = 32 * q + lane;
         const uint32_t t_lane = uint32_t(32 * q) << 16;
-        const uint32_t acce0 = mapa_shared(&acce[0], 0);
+        const uint32_t acce0 = PAIR ? mapa_shared(&acce[0], 0) : 0u;
         uint32_t tc = 0;
         bool ok = true;
         for (int64_t w = cluster; ok && w < num_tiles; w += nclusters, ++tc) {
@@ -455,26 +478,30 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive_cluster(acce0 + buf * 8);
+            if (lane == 0) {
+                if constexpr (PAIR) mbar_arrive_cluster(acce0 + buf * 8); else mbar_arrive(&acce[buf]);
+            }
         }
         if (!ok && lane == 0) mx_record(FP8_ERR_TIMEOUT);
     }
 
     tc_fence_before();
     __syncthreads();
-    cluster_sync();
+    if constexpr (PAIR) cluster_sync();
     if (warp == 1) {
         tc_fence_after();
-        tmem_dealloc_pair(tmem_base, kTmemCols);
+        if constexpr (PAIR) tmem_dealloc_pair(tmem_base, kTmemCols); else tmem_dealloc(tmem_base, kTmemCols);
     }
 }
 
-constexpr int kStages = 7;
+constexpr int kStages = 7;           // a pair: 30 KB of operands per stage and CTA
+constexpr int kSingleStages = 4;     // one CTA: 44 KB per stage
 
-template <int BMODE, bool OUT_F32, bool GROUPED>
+template <bool PAIR, int BMODE, bool OUT_F32, bool GROUPED>
 static int launch(const CUtensorMap& ma, const CUtensorMap& mb, const Args& args, int sms, cudaStream_t stream) {
-    using Lay = Layout<kStages, GROUPED>;
-    auto kern = gemm_mx_pair_kernel<kStages, BMODE, OUT_F32, GROUPED>;
+    constexpr int S = PAIR ? kStages : kSingleStages;
+    using Lay = Layout<PAIR, S, GROUPED>;
+    auto kern = gemm_mx_pair_kernel<PAIR, S, BMODE, OUT_F32, GROUPED>;
     static bool attr_set = false;
     if (!attr_set) {
         if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Lay::kDynSmem) != cudaSuccess)
@@ -490,6 +517,12 @@ static int launch(const CUtensorMap& ma, const CUtensorMap& mb, const Args& args
     cfg.blockDim = dim3(kThreads);
     cfg.dynamicSmemBytes = Lay::kDynSmem;
     cfg.stream = stream;
+    if constexpr (!PAIR) {
+        // one CTA per SM (shared memory and launch bounds allow no more)
+        cfg.gridDim = dim3(sms);
+        if (cudaLaunchKernelEx(&cfg, kern, ma, mb, args) != cudaSuccess) return FP8_ERR_CUDA;
+        return cudaGetLastError() == cudaSuccess ? FP8_OK : FP8_ERR_CUDA;
+    }
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     int max_clusters = 0;
@@ -528,11 +561,11 @@ extern "C" int fp8_gemm_blockscaled_pow2(const uint8_t* a, const float* sa, cons
     const int grid_sms = int(2 * pair_tiles < sms ? 2 * pair_tiles : sms);
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     if (b_scale_mode == FP8_BSCALE_BLOCK128) {
-        if (d_dtype == FP8_OUT_BF16) return mx::launch<0, false, false>(ma, mb, args, grid_sms, s);
-        return mx::launch<0, true, false>(ma, mb, args, grid_sms, s);
+        if (d_dtype == FP8_OUT_BF16) return mx::launch<true, 0, false, false>(ma, mb, args, grid_sms, s);
+        return mx::launch<true, 0, true, false>(ma, mb, args, grid_sms, s);
     }
-    if (d_dtype == FP8_OUT_BF16) return mx::launch<1, false, false>(ma, mb, args, grid_sms, s);
-    return mx::launch<1, true, false>(ma, mb, args, grid_sms, s);
+    if (d_dtype == FP8_OUT_BF16) return mx::launch<true, 1, false, false>(ma, mb, args, grid_sms, s);
+    return mx::launch<true, 1, true, false>(ma, mb, args, grid_sms, s);
 }
 
 extern "C" int fp8_grouped_gemm_blockscaled_pow2(const uint8_t* a, const float* sa, const uint8_t* b, const float* sb,
@@ -548,8 +581,8 @@ extern "C" int fp8_grouped_gemm_blockscaled_pow2(const uint8_t* a, const float* 
     if (!aligned16(a) || !aligned16(b) || !aligned16(d) || !aligned16(sa) || !aligned16(sb) ||
         (reinterpret_cast<uintptr_t>(expert_offsets) & 3u))
         return FP8_ERR_ALIGN;
-    // at most total_rows/256 + E row pairs, each with ceil(N/224) column tiles of K/128 blocks
-    const int64_t max_tiles = (total_rows / (2 * mx::BM) + E) * ((N + mx::BN - 1) / mx::BN);
+    // at most total_rows/128 + E row tiles, each with ceil(N/224) column tiles of K/128 blocks
+    const int64_t max_tiles = (total_rows / mx::BM + E) * ((N + mx::BN - 1) / mx::BN);
     if (max_tiles * (K / 128) >= (int64_t(1) << 31) || int64_t(E) * (N / 128) * (K / 128) >= (int64_t(1) << 31) ||
         N + mx::BN >= (int64_t(1) << 31))
         return FP8_ERR_SHAPE;
@@ -557,10 +590,12 @@ extern "C" int fp8_grouped_gemm_blockscaled_pow2(const uint8_t* a, const float* 
     if (sms <= 0) return FP8_ERR_DEVICE;
     CUtensorMap ma, mb;
     if (!make_operand_map(&ma, a, total_rows, K, mx::BM, 1, false) ||
-        !make_operand_map(&mb, b, N, K, mx::BN / 2, E, true))
+        !make_operand_map(&mb, b, N, K, mx::BN, E, true))
         return FP8_ERR_CUDA;
     const mx::Args args{sa, sb, d, total_rows, N, K, expert_offsets, E};
-    return mx::launch<0, false, true>(ma, mb, args, sms, reinterpret_cast<cudaStream_t>(stream));
+    // one CTA per 128 x 224 tile: experts hold ~128 rows on average, so a
+    // 256-row pair tile would spend half its MMAs on padding rows
+    return mx::launch<false, 0, false, true>(ma, mb, args, sms, reinterpret_cast<cudaStream_t>(stream));
 }
 
 // Status word of this translation unit: read and clear (synchronising).
