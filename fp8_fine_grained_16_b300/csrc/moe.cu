@@ -209,7 +209,11 @@ __global__ void __launch_bounds__(256) permute_rows_kernel(const uint8_t* __rest
 // ------------------------------------------------------------------ combine
 // Thread = (token t, 8 consecutive columns).  Consecutive threads take
 // consecutive column groups of one token, so every y row is read in full
-// 16-byte pieces and the output row is written coalesced.
+// 16-byte pieces and the output row is written coalesced.  With KC > 0 the
+// token's k = KC positions and gates are loaded first and then all KC rows
+// at once, so the row loads are in flight together; the sum runs in slot
+// order either way.
+template <int KC>
 __global__ void __launch_bounds__(256) moe_combine_kernel(const uint16_t* __restrict__ y, int64_t rows,
                                                          const int32_t* __restrict__ pos,
                                                          const float* __restrict__ gate, int64_t T, int k, int64_t N,
@@ -222,19 +226,48 @@ __global__ void __launch_bounds__(256) moe_combine_kernel(const uint16_t* __rest
         float acc[8];
 #pragma unroll
         for (int i = 0; i < 8; ++i) acc[i] = 0.0f;
-        for (int j = 0; j < k; ++j) {
-            const int32_t p = __ldg(pos + t * k + j);
-            const float w = __ldg(gate + t * k + j);
-            if (p < 0 || p >= rows) {
-                moe_record(FP8_ERR_OFFSETS);
-                continue;
-            }
-            const uint4 v = __ldg(reinterpret_cast<const uint4*>(y + int64_t(p) * N) + g);
-            const uint32_t ww[4] = {v.x, v.y, v.z, v.w};
+        if constexpr (KC > 0) {
+            int32_t p[KC];
+            float w[KC];
+            uint4 v[KC];
 #pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                acc[2 * i] = fmaf(w, bf16_lo(ww[i]), acc[2 * i]);
-                acc[2 * i + 1] = fmaf(w, bf16_hi(ww[i]), acc[2 * i + 1]);
+            for (int j = 0; j < KC; ++j) {
+                p[j] = __ldg(pos + t * KC + j);
+                w[j] = __ldg(gate + t * KC + j);
+            }
+#pragma unroll
+            for (int j = 0; j < KC; ++j) {
+                const bool ok = p[j] >= 0 && p[j] < rows;
+                v[j] = ok ? __ldg(reinterpret_cast<const uint4*>(y + int64_t(p[j]) * N) + g) : make_uint4(0, 0, 0, 0);
+            }
+#pragma unroll
+            for (int j = 0; j < KC; ++j) {
+                if (p[j] < 0 || p[j] >= rows) {
+                    moe_record(FP8_ERR_OFFSETS);
+                    continue;
+                }
+                const uint32_t ww[4] = {v[j].x, v[j].y, v[j].z, v[j].w};
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    acc[2 * i] = fmaf(w[j], bf16_lo(ww[i]), acc[2 * i]);
+                    acc[2 * i + 1] = fmaf(w[j], bf16_hi(ww[i]), acc[2 * i + 1]);
+                }
+            }
+        } else {
+            for (int j = 0; j < k; ++j) {
+                const int32_t p = __ldg(pos + t * k + j);
+                const float w = __ldg(gate + t * k + j);
+                if (p < 0 || p >= rows) {
+                    moe_record(FP8_ERR_OFFSETS);
+                    continue;
+                }
+                const uint4 v = __ldg(reinterpret_cast<const uint4*>(y + int64_t(p) * N) + g);
+                const uint32_t ww[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    acc[2 * i] = fmaf(w, bf16_lo(ww[i]), acc[2 * i]);
+                    acc[2 * i + 1] = fmaf(w, bf16_hi(ww[i]), acc[2 * i + 1]);
+                }
             }
         }
         reinterpret_cast<uint4*>(out + t * N)[g] =
@@ -314,8 +347,12 @@ extern "C" int fp8_moe_combine_bf16(const uint16_t* y, int64_t rows, const int32
     const int64_t total = T * (N / 8);
     const int64_t blocks = (total + 255) / 256;
     const int64_t cap = int64_t(sm_count()) * 8;
-    moe_combine_kernel<<<unsigned(blocks < cap ? blocks : cap), 256, 0, reinterpret_cast<cudaStream_t>(stream)>>>(
-        y, rows, pos, gate, T, topk, N, out);
+    const unsigned grid = unsigned(blocks < cap ? blocks : cap);
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    if (topk == 8)
+        moe_combine_kernel<8><<<grid, 256, 0, st>>>(y, rows, pos, gate, T, topk, N, out);
+    else
+        moe_combine_kernel<0><<<grid, 256, 0, st>>>(y, rows, pos, gate, T, topk, N, out);
     return cudaGetLastError() == cudaSuccess ? FP8_OK : FP8_ERR_CUDA;
 }
 
