@@ -12,9 +12,11 @@
 // loads the 32-bit words at byte column 4l of the input rows 4q .. 4q+3
 // (q = w + 8j, j < 4): every load instruction of a warp reads whole 128-byte
 // rows.  Each 4x4 byte block is transposed in registers (byte permutes) and
-// lands in a shared tile whose word index is rotated by the writing lane, so
-// neither the stores nor the loads of shared memory conflict; the output
-// leaves as 16-byte pieces of whole 128-byte rows.
+// lands in a shared tile whose word index is rotated per output row c by
+// (c/4 + 4*(c%4)) mod 32, which keeps both the stores (a warp writes rows
+// c = 4*lane + i) and the loads (a warp reads 16 consecutive rows, two
+// threads per row) on 32 distinct banks; the output leaves as 16-byte pieces
+// of whole 128-byte rows.
 #include "common.cuh"
 
 namespace fp8bs {
@@ -37,7 +39,7 @@ __global__ void __launch_bounds__(256) transpose_128x128_kernel(const uint8_t* _
                                                                 int64_t K, uint8_t* __restrict__ qT,
                                                                 float* __restrict__ sT) {
     // T[c][slot]: output row c (= input column), 32 words = input rows 4*word ..
-    // 4*word+3; word `wd` of row c sits at slot (wd + c/4) % 32.
+    // 4*word+3; word `wd` of row c sits at slot (wd + c/4 + 4*(c%4)) % 32.
     __shared__ uint32_t T[128 * 32];
     const int64_t nkb = K >> 7, nnb = N >> 7;
     const int64_t nb = blockIdx.x / nkb, kb = blockIdx.x - nb * nkb;
@@ -55,7 +57,7 @@ __global__ void __launch_bounds__(256) transpose_128x128_kernel(const uint8_t* _
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
             const int c = 4 * lane + i;                    // input column = output row
-            T[c * 32 + ((qd + lane) & 31)] = out[i];
+            T[c * 32 + ((qd + lane + 4 * i) & 31)] = out[i];   // c/4 = lane, c%4 = i
         }
     }
     __syncthreads();
@@ -68,7 +70,7 @@ __global__ void __launch_bounds__(256) transpose_128x128_kernel(const uint8_t* _
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
             const int wd = 16 * h + 4 * v + e;
-            w[e] = T[c * 32 + ((wd + (c >> 2)) & 31)];
+            w[e] = T[c * 32 + ((wd + (c >> 2) + 4 * (c & 3)) & 31)];
         }
         reinterpret_cast<uint4*>(dst)[v] = make_uint4(w[0], w[1], w[2], w[3]);
     }
