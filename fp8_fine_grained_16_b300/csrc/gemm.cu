@@ -31,13 +31,23 @@
 //   warps 4..11   promotion: two warpgroups, one per 128-column half.  Thread
 //                 (warp w, lane l) owns row 32*(w%4)+l of its CTA's 128 rows
 //                 (TMEM lanes are tied to w%4).  Per K block it reads P_kb
-//                 from TMEM 32 columns at a time, frees the accumulator once
+//                 from TMEM in two 64-column loads, frees the accumulator once
 //                 all of it is in registers, and adds P_kb * sA*sB into 128
-//                 fp32 registers with packed two-lane FMAs.
+//                 fp32 registers with packed two-lane FMAs.  It frees a stage
+//                 as soon as the scales it needs are in its own shared-memory
+//                 slots.
 //
 // The kernel is persistent: each cluster walks a static list of pair tiles;
 // stage and accumulator indices run on across tile boundaries, so the
 // epilogue of one tile overlaps the first MMAs of the next.
+//
+// Tail split (dense forms).  When the tiles leave a last wave of
+// at most half the clusters, those tail tiles are cut along K instead: each
+// cluster, after its whole-K tiles, promotes one K range of one tail tile
+// and writes that fp32 partial sum to a workspace slab.  A second kernel on
+// the same stream adds a tile's slabs in K order and stores D (or quantises
+// it, for the E4M3 output).  The result is the same sum of promoted K blocks,
+// regrouped into per-range fp32 sums.
 //
 // Every pipeline wait is bounded (2 s).  A wait that expires records
 // FP8_ERR_TIMEOUT in the device status word, raises the CTA's abort flag,
@@ -81,6 +91,9 @@ struct GemmArgs {
     int E;                   // grouped only
     float* s_out;            // E4M3 output: 1x128 scales of D, [N/128][M]
     uint32_t flags;          // E4M3 output: FP8_SCALE_POW2
+    float* ws = nullptr;     // tail split: [tail tiles * split][256][256] fp32 partial sums
+    int64_t tail0 = 0;       // tail split: first split tile; tiles below it run over the whole K
+    int32_t split = 0;       // tail split: K ranges per tail tile (0: no split)
 };
 
 // Output forms of the GEMM.
@@ -115,7 +128,8 @@ struct Tile {
 //                        promotion warp pre-arrives on full[0] and full[1]).
 //   sfull[s] (each)    = producer's arrival + this CTA's scale bytes + the
 //                        MMA commit of that K block (its accumulator is ready).
-//   empty[s] (each)    = MMA commit + this CTA's 8 promotion warps.
+//   empty[s] (each)    = MMA commit + this CTA's 8 promotion warps (each
+//                        arrives once it has copied the scales it reads).
 constexpr int kPairStages = 6;
 constexpr int kSingleStages = 4;     // one CTA holds all 256 B rows: 48 KB of operands per stage
 // Register split (launched with 168 per thread, 64512 in all): warpgroup 0
@@ -140,7 +154,15 @@ struct PairLayout {
     static constexpr int kBarOff = kStagesBytes;  // full[S], sfull[S], empty[S], done
     static constexpr int kNumBars = 3 * STAGES + 1;
     static constexpr int kMiscOff = kBarOff + kNumBars * 8;       // tmem base, abort flag
-    static constexpr int kGrpOff = (kMiscOff + 16 + 15) & ~15;
+    // Promotion warps' own copies of the scales they read from a stage (so the
+    // stage can be freed at once): per warp, a slot per lane for its row scale
+    // or scale product, and in BMODE 1 two buffers of its half's 128 column
+    // scales (alternating K blocks).
+    static constexpr int kPrivOff = (kMiscOff + 16 + 15) & ~15;
+    static constexpr int kPrivRowBytes = kPromoWarps * 32 * 4;
+    static constexpr int kPrivColOff = kPrivOff + kPrivRowBytes;
+    static constexpr int kPrivColBytes = BMODE == 1 ? 2 * kPromoWarps * (BN / 2) * 4 : 0;
+    static constexpr int kGrpOff = kPrivColOff + kPrivColBytes;
     static constexpr int kGrpBytes = GROUPED ? 2 * (kMaxExperts + 1) * 4 : 0;
     static constexpr int kBytes = kGrpOff + kGrpBytes;
     static constexpr int kDynSmem = kBytes + 1024;
@@ -271,6 +293,22 @@ __global__ void __launch_bounds__(kThreads, 1)
     };
     int64_t num_tiles;
     if constexpr (GROUPED) num_tiles = gs.count(); else num_tiles = ds.count();
+    // This cluster's work units: the tiles w = cluster + i * nclusters below
+    // the split tiles (whole K), then, under a tail split, K range s of split
+    // tile j, where cluster = j * split + s (its workspace slab).
+    struct Unit {
+        int64_t w, kb0, kb1;
+        int64_t slab;            // < 0: whole tile, stored to D
+    };
+    const bool splitting = !GROUPED && args.split > 0;
+    const int64_t whole_end = splitting ? args.tail0 : num_tiles;
+    const int64_t n_whole = whole_end > cluster ? (whole_end - cluster + nclusters - 1) / nclusters : 0;
+    const int64_t n_units = n_whole + ((splitting && cluster < (num_tiles - args.tail0) * args.split) ? 1 : 0);
+    auto unit_at = [&](int64_t i) -> Unit {
+        if (i < n_whole) return Unit{cluster + i * nclusters, 0, nkb, -1};
+        const int64_t j = cluster / args.split, sp = cluster % args.split;
+        return Unit{args.tail0 + j, sp * nkb / args.split, (sp + 1) * nkb / args.split, cluster};
+    };
     auto sb_row = [&](const Tile& t, int h) -> int64_t {
         const int64_t c0 = int64_t(t.n0) + h * kHalf;
         return (int64_t(t.e) * (args.N / 128) + (c0 < args.N ? c0 : args.N - 1) / 128) * nkb;
@@ -284,14 +322,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const uint32_t full0 = PAIR ? mapa_shared(&full[0], 0) : 0u;   // leader's full[0], cluster address
                 uint32_t it = 0;
                 bool ok = true;
-                for (int64_t w = cluster; ok && w < num_tiles; w += nclusters) {
-                    const Tile t = tile_at(w);
+                for (int64_t ui = 0; ok && ui < n_units; ++ui) {
+                    const Unit u = unit_at(ui);
+                    const Tile t = tile_at(u.w);
                     int64_t sbr[2] = {0, 0};
                     if constexpr (BMODE == 0) {
                         sbr[0] = sb_row(t, 0);
                         sbr[1] = sb_row(t, 1);
                     }
-                    for (int64_t kb = 0; kb < nkb; ++kb) {
+                    for (int64_t kb = u.kb0; kb < u.kb1; ++kb) {
                         const uint32_t stage = it % STAGES, phase = (it / STAGES) & 1u;
                         if (!mbar_wait_bounded(&empty[stage], phase ^ 1u, abort_s)) {
                             ok = false;
@@ -345,8 +384,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (leader && lane == 0) {
                 uint32_t it = 0, g = 0;
                 bool ok = true;
-                for (int64_t w = cluster; ok && w < num_tiles; w += nclusters) {
-                    for (int64_t kb = 0; kb < nkb; ++kb) {
+                for (int64_t ui = 0; ok && ui < n_units; ++ui) {
+                    const Unit u = unit_at(ui);
+                    for (int64_t kb = u.kb0; kb < u.kb1; ++kb) {
                         const uint32_t buf = g & 1u;
                         const uint32_t stage = it % STAGES, phase = (it / STAGES) & 1u;
                         // operands of both CTAs landed and accumulator `buf` is free
@@ -403,8 +443,9 @@ __global__ void __launch_bounds__(kThreads, 1)
 
         uint32_t g = 0;
         bool ok = true;
-        for (int64_t w = cluster; ok && w < num_tiles; w += nclusters) {
-            const Tile t = tile_at(w);
+        for (int64_t ui = 0; ok && ui < n_units; ++ui) {
+            const Unit u = unit_at(ui);
+            const Tile t = tile_at(u.w);
             // Where this K block's scales sit in the stage's boxes: the sA box
             // starts at (kb*M + row0) rounded down to 4 elements, the BMODE-0 sB
             // box at (sb_row + kb) rounded down to 4.  Both offsets advance by a
@@ -416,7 +457,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
             for (int i = 0; i < kHalf / 2; ++i) acc[i] = make_float2(0.0f, 0.0f);
 
-            for (int kb = 0; kb < int(nkb); ++kb) {
+            for (int kb = int(u.kb0); kb < int(u.kb1); ++kb) {
                 const uint32_t stage = g % STAGES, phase = (g / STAGES) & 1u;
                 const uint32_t buf = g & 1u;
                 // scales landed and the MMAs of this K block are done
@@ -431,15 +472,33 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const float sa_cur = reinterpret_cast<const float*>(st + L::kSaOff)[((sa_off0 + kb * m_step) & 3) + r];
                 const float2 sa2 = make_float2(sa_cur, sa_cur);
                 float2 sc2 = sa2;
-                const float* sbk = reinterpret_cast<const float*>(st + L::kSbOff) + half * kHalf;
+                // The warp frees the stage as soon as it has its scales.  Every
+                // value it read from the stage first goes into a shared-memory
+                // store of its own (a store cannot be made before its load
+                // completes, and the release arrive orders it), so the stage's
+                // next TMA refill cannot overtake a read.  Freeing the stage
+                // while a read was still only feeding later FMAs let the refill
+                // overwrite column scales not yet read: results varied from
+                // run to run.
+                float* row_slot = reinterpret_cast<float*>(smem + L::kPrivOff) + (warp - 4) * 32 + lane;
+                const float* sbk = reinterpret_cast<const float*>(smem + L::kPrivColOff) +
+                                   ((g & 1u) * kPromoWarps + (warp - 4)) * kHalf;
                 if constexpr (BMODE == 0) {
                     const float sbv =
                         reinterpret_cast<const float*>(st + L::kSbOff)[half * kSbHalf0 + ((sb_off0 + kb) & 3)];
                     const float sc = __fmul_rn(sa_cur, sbv);
                     sc2 = make_float2(sc, sc);
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive(&empty[stage]);
+                    *row_slot = sc;
+                } else {
+                    // this K block's copy of the half's column scales (buffer g % 2,
+                    // last read two K blocks ago): one 16-byte piece per lane
+                    const float4 b4 =
+                        reinterpret_cast<const float4*>(reinterpret_cast<const float*>(st + L::kSbOff) + half * kHalf)[lane];
+                    reinterpret_cast<float4*>(const_cast<float*>(sbk))[lane] = b4;
+                    *row_slot = sa_cur;
                 }
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&empty[stage]);
 
                 auto scale_chunk = [&](int c, const uint32_t* v) {
                     if constexpr (BMODE == 0) {
@@ -483,14 +542,23 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (lane == 0) release((g + 2) % STAGES);
                 scale_chunk(2, v);
                 scale_chunk(3, v + 32);
-                if constexpr (BMODE == 1) {
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive(&empty[stage]);
-                }
                 ++g;
             }
             if (!ok) break;
 
+            if constexpr (!GROUPED) {
+                if (u.slab >= 0) {
+                    // K range of a split tile: the whole 256 x 256 partial goes
+                    // to its slab (rows and columns past D included); the
+                    // fix-up kernel adds the slabs and applies the bounds
+                    float* dst = args.ws + (u.slab * kTileRows + int64_t(rank) * BM + r) * BN + half * kHalf;
+#pragma unroll
+                    for (int i = 0; i < kHalf / 2; i += 2)
+                        *reinterpret_cast<float4*>(dst + 2 * i) =
+                            make_float4(acc[i].x, acc[i].y, acc[i + 1].x, acc[i + 1].y);
+                    continue;
+                }
+            }
             const int64_t m = t.row0 + r;
             const int64_t ncol0 = int64_t(t.n0) + half * kHalf;
             if (ncol0 < args.N && m < t.row_end && m < args.M) {
@@ -549,12 +617,65 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
 }
 
+// Tail split fix-up: D over the split tiles = the sum of each tile's slabs,
+// added in K order in fp32, then stored as the GEMM stores it.  Block b
+// covers rows 4 * (b % 64) .. +3 of split tile b / 64; a thread adds four
+// columns, so a warp holds one row x 128 columns: for the E4M3 output that
+// is one 1x128 tile, quantised as the GEMM's epilogue does (amax over the
+// warp, the same scale rule and conversion).
+constexpr int kFixRowsPerBlock = 4;
+template <int OUT>
+__global__ void __launch_bounds__(256) splitk_fixup_kernel(const float* __restrict__ ws, void* __restrict__ d,
+                                                          int64_t M, int64_t N, int64_t tail0, int split,
+                                                          int64_t num_m2, float* __restrict__ s_out,
+                                                          uint32_t flags) {
+    constexpr int kTile = 256;
+    const int64_t j = blockIdx.x / (kTile / kFixRowsPerBlock);
+    const int row = int(blockIdx.x % (kTile / kFixRowsPerBlock)) * kFixRowsPerBlock + int(threadIdx.x >> 6);
+    const int c = int(threadIdx.x & 63) * 4;
+    const int64_t w = tail0 + j;
+    const int64_t m = (w % num_m2) * kTile + row, n = (w / num_m2) * kTile + c;
+    // a warp's 32 threads share m and the 128-column block of n: they leave together
+    if (m >= M || n >= N) return;
+    const float4* p = reinterpret_cast<const float4*>(ws + (j * split * kTile + row) * kTile + c);
+    constexpr int64_t kSlab = int64_t(kTile) * kTile / 4;      // float4s per slab
+    float4 acc = p[0];
+#pragma unroll 4
+    for (int sp = 1; sp < split; ++sp) {
+        const float4 v = p[sp * kSlab];
+        acc = make_float4(__fadd_rn(acc.x, v.x), __fadd_rn(acc.y, v.y), __fadd_rn(acc.z, v.z), __fadd_rn(acc.w, v.w));
+    }
+    if constexpr (OUT == kOutE4M3) {
+        float amax = fmaxf(fmaxf(fabsf(acc.x), fabsf(acc.y)), fmaxf(fabsf(acc.z), fabsf(acc.w)));
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, o));
+        float inv;
+        const float sc = tile_scale(amax, (flags & FP8_SCALE_POW2) != 0, inv);
+        *reinterpret_cast<uint32_t*>(reinterpret_cast<uint8_t*>(d) + m * N + n) =
+            cvt_e4m3x2(__fmul_rn(acc.x, inv), __fmul_rn(acc.y, inv)) |
+            (cvt_e4m3x2(__fmul_rn(acc.z, inv), __fmul_rn(acc.w, inv)) << 16);
+        if ((threadIdx.x & 31) == 0) s_out[(n / 128) * M + m] = sc;
+    } else if constexpr (OUT == kOutF32) {
+        *reinterpret_cast<float4*>(reinterpret_cast<float*>(d) + m * N + n) = acc;
+    } else {
+        *reinterpret_cast<uint2*>(reinterpret_cast<uint16_t*>(d) + m * N + n) =
+            make_uint2(cvt_bf16x2(acc.x, acc.y), cvt_bf16x2(acc.z, acc.w));
+    }
+}
+
 // ---------------------------------------------------------------- host side
 constexpr int kBN = 256;
+constexpr int kSplitMinKBlocks = 16;                 // below this a split saves less than the fix-up costs
+constexpr int64_t kSlabBytes = int64_t(2 * BM) * kBN * 4;
+
+// Workspace the tail split may use on this device: one slab per cluster.
+static int64_t split_workspace_bytes(int sms, int64_t K) {
+    return K / 128 >= kSplitMinKBlocks ? int64_t(sms / 2) * kSlabBytes : 0;
+}
 
 template <bool PAIR, int BN, int STAGES, int BMODE, int OUT, bool GROUPED>
 static int launch_pair(const CUtensorMap& ma, const CUtensorMap& mb, const CUtensorMap& msa, const CUtensorMap& msb,
-                       const GemmArgs& args, int sms, cudaStream_t stream) {
+                       GemmArgs args, int sms, cudaStream_t stream, int64_t ws_bytes = 0) {
     using L = PairLayout<PAIR, BN, STAGES, BMODE, GROUPED>;
     auto kern = gemm_pair_kernel<PAIR, BN, STAGES, BMODE, OUT, GROUPED>;
     static bool attr_set = false;
@@ -584,9 +705,38 @@ static int launch_pair(const CUtensorMap& ma, const CUtensorMap& mb, const CUten
     cfg.gridDim = dim3(2 * (sms / 2));
     if (cudaOccupancyMaxActiveClusters(&max_clusters, kern, &cfg) != cudaSuccess || max_clusters <= 0)
         return FP8_ERR_CUDA;
-    const int clusters = max_clusters < sms / 2 ? max_clusters : sms / 2;
+    int clusters = max_clusters < sms / 2 ? max_clusters : sms / 2;
+    // Tail split: a last wave of at most half the clusters is cut along K,
+    // one K range per cluster (so the slabs never exceed one per cluster).
+    // Every launched cluster gets work: when all tiles are split, exactly
+    // one cluster per K range; without a split, at most one per tile.
+    args.split = 0;
+    int64_t num_m2 = 0, n_tail = 0;
+    if constexpr (PAIR && !GROUPED) {
+        num_m2 = (args.M + 2 * BM - 1) / (2 * BM);
+        const int64_t num_tiles = num_m2 * ((args.N + BN - 1) / BN);
+        const int64_t nkb = args.K / BK;
+        n_tail = num_tiles % clusters;
+        if (args.ws && nkb >= kSplitMinKBlocks && n_tail > 0 && 2 * n_tail <= clusters) {
+            int64_t sp = clusters / n_tail;
+            if (sp > nkb / 2) sp = nkb / 2;
+            if (n_tail * sp * kSlabBytes <= ws_bytes) {
+                args.split = int32_t(sp);
+                args.tail0 = num_tiles - n_tail;
+                if (args.tail0 == 0) clusters = int(n_tail * sp);
+            }
+        }
+        if (args.split == 0 && num_tiles < clusters) clusters = int(num_tiles);
+    }
     cfg.gridDim = dim3(2 * clusters);
     if (cudaLaunchKernelEx(&cfg, kern, ma, mb, msa, msb, args) != cudaSuccess) return FP8_ERR_CUDA;
+    if constexpr (PAIR && !GROUPED) {
+        if (args.split > 0) {
+            const unsigned blocks = unsigned(n_tail * (2 * BM / kFixRowsPerBlock));
+            splitk_fixup_kernel<OUT><<<blocks, 256, 0, stream>>>(args.ws, args.d, args.M, args.N, args.tail0,
+                                                                  args.split, num_m2, args.s_out, args.flags);
+        }
+    }
     return cudaGetLastError() == cudaSuccess ? FP8_OK : FP8_ERR_CUDA;
 }
 
@@ -608,9 +758,9 @@ __global__ void wait_timeout_selftest_kernel(uint64_t timeout_ns) {
 
 using namespace fp8bs;
 
-extern "C" int fp8_gemm_blockscaled(const uint8_t* a, const float* sa, const uint8_t* b, const float* sb,
-                                    int b_scale_mode, void* d, int d_dtype, int64_t M, int64_t N, int64_t K,
-                                    fp8_stream_t stream) {
+static int gemm_blockscaled_impl(const uint8_t* a, const float* sa, const uint8_t* b, const float* sb,
+                                 int b_scale_mode, void* d, int d_dtype, int64_t M, int64_t N, int64_t K,
+                                 float* ws, int64_t ws_bytes, fp8_stream_t stream) {
     if (!a || !sa || !b || !sb || !d || M <= 0 || N <= 0 || K <= 0) return FP8_ERR_ARG;
     if ((b_scale_mode != FP8_BSCALE_BLOCK128 && b_scale_mode != FP8_BSCALE_ROW) ||
         (d_dtype != FP8_OUT_BF16 && d_dtype != FP8_OUT_F32))
@@ -629,20 +779,49 @@ extern "C" int fp8_gemm_blockscaled(const uint8_t* a, const float* sa, const uin
         !make_scale_map(&msb, sb, nsb, b_scale_mode == FP8_BSCALE_ROW ? kBN : kSbBox0))
         return FP8_ERR_CUDA;
     GemmArgs args{sa, sb, d, nullptr, M, N, K, 0, nullptr, 0u};
+    args.ws = ws;
     const int64_t pair_tiles = ((M + 2 * BM - 1) / (2 * BM)) * ((N + kBN - 1) / kBN);
-    const int grid_sms = int(2 * pair_tiles < sms ? 2 * pair_tiles : sms);
+    // with a workspace, fewer tiles than clusters are split along K over the
+    // whole GPU; without one, a cluster per tile
+    const bool may_split = ws && K / 128 >= kSplitMinKBlocks;
+    const int grid_sms = int(may_split || 2 * pair_tiles >= sms ? sms : 2 * pair_tiles);
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     if (b_scale_mode == FP8_BSCALE_BLOCK128) {
-        if (d_dtype == FP8_OUT_BF16) return launch_pair<true, kBN, kPairStages, 0, kOutBF16, false>(ma, mb, msa, msb, args, grid_sms, s);
-        return launch_pair<true, kBN, kPairStages, 0, kOutF32, false>(ma, mb, msa, msb, args, grid_sms, s);
+        if (d_dtype == FP8_OUT_BF16)
+            return launch_pair<true, kBN, kPairStages, 0, kOutBF16, false>(ma, mb, msa, msb, args, grid_sms, s, ws_bytes);
+        return launch_pair<true, kBN, kPairStages, 0, kOutF32, false>(ma, mb, msa, msb, args, grid_sms, s, ws_bytes);
     }
-    if (d_dtype == FP8_OUT_BF16) return launch_pair<true, kBN, kPairStages, 1, kOutBF16, false>(ma, mb, msa, msb, args, grid_sms, s);
-    return launch_pair<true, kBN, kPairStages, 1, kOutF32, false>(ma, mb, msa, msb, args, grid_sms, s);
+    if (d_dtype == FP8_OUT_BF16)
+        return launch_pair<true, kBN, kPairStages, 1, kOutBF16, false>(ma, mb, msa, msb, args, grid_sms, s, ws_bytes);
+    return launch_pair<true, kBN, kPairStages, 1, kOutF32, false>(ma, mb, msa, msb, args, grid_sms, s, ws_bytes);
 }
 
-extern "C" int fp8_gemm_blockscaled_q8(const uint8_t* a, const float* sa, const uint8_t* b, const float* sb,
-                                       int b_scale_mode, uint8_t* q_out, float* s_out, uint32_t flags, int64_t M,
-                                       int64_t N, int64_t K, fp8_stream_t stream) {
+extern "C" int fp8_gemm_blockscaled(const uint8_t* a, const float* sa, const uint8_t* b, const float* sb,
+                                    int b_scale_mode, void* d, int d_dtype, int64_t M, int64_t N, int64_t K,
+                                    fp8_stream_t stream) {
+    return gemm_blockscaled_impl(a, sa, b, sb, b_scale_mode, d, d_dtype, M, N, K, nullptr, 0, stream);
+}
+
+extern "C" int64_t fp8_gemm_blockscaled_workspace_bytes(int64_t M, int64_t N, int64_t K) {
+    if (M <= 0 || N <= 0 || K <= 0) return FP8_ERR_ARG;
+    const int sms = device_sms();
+    if (sms <= 0) return FP8_ERR_DEVICE;
+    return split_workspace_bytes(sms, K);
+}
+
+extern "C" int fp8_gemm_blockscaled_ws(const uint8_t* a, const float* sa, const uint8_t* b, const float* sb,
+                                       int b_scale_mode, void* d, int d_dtype, int64_t M, int64_t N, int64_t K,
+                                       void* workspace, int64_t workspace_bytes, fp8_stream_t stream) {
+    if (workspace_bytes < 0 || (workspace_bytes > 0 && !workspace)) return FP8_ERR_ARG;
+    if (workspace && !aligned16(workspace)) return FP8_ERR_ALIGN;
+    return gemm_blockscaled_impl(a, sa, b, sb, b_scale_mode, d, d_dtype, M, N, K,
+                                 workspace_bytes > 0 ? static_cast<float*>(workspace) : nullptr, workspace_bytes,
+                                 stream);
+}
+
+static int gemm_blockscaled_q8_impl(const uint8_t* a, const float* sa, const uint8_t* b, const float* sb,
+                                    int b_scale_mode, uint8_t* q_out, float* s_out, uint32_t flags, int64_t M,
+                                    int64_t N, int64_t K, float* ws, int64_t ws_bytes, fp8_stream_t stream) {
     if (!a || !sa || !b || !sb || !q_out || !s_out || M <= 0 || N <= 0 || K <= 0) return FP8_ERR_ARG;
     if ((b_scale_mode != FP8_BSCALE_BLOCK128 && b_scale_mode != FP8_BSCALE_ROW) || (flags & ~FP8_SCALE_POW2))
         return FP8_ERR_ARG;
@@ -663,12 +842,31 @@ extern "C" int fp8_gemm_blockscaled_q8(const uint8_t* a, const float* sa, const 
         !make_scale_map(&msb, sb, nsb, b_scale_mode == FP8_BSCALE_ROW ? kBN : kSbBox0))
         return FP8_ERR_CUDA;
     GemmArgs args{sa, sb, q_out, nullptr, M, N, K, 0, s_out, flags};
+    args.ws = ws;
     const int64_t pair_tiles = ((M + 2 * BM - 1) / (2 * BM)) * ((N + kBN - 1) / kBN);
-    const int grid_sms = int(2 * pair_tiles < sms ? 2 * pair_tiles : sms);
+    const bool may_split = ws && K / 128 >= kSplitMinKBlocks;
+    const int grid_sms = int(may_split || 2 * pair_tiles >= sms ? sms : 2 * pair_tiles);
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     if (b_scale_mode == FP8_BSCALE_BLOCK128)
-        return launch_pair<true, kBN, kPairStages, 0, kOutE4M3, false>(ma, mb, msa, msb, args, grid_sms, s);
-    return launch_pair<true, kBN, kPairStages, 1, kOutE4M3, false>(ma, mb, msa, msb, args, grid_sms, s);
+        return launch_pair<true, kBN, kPairStages, 0, kOutE4M3, false>(ma, mb, msa, msb, args, grid_sms, s, ws_bytes);
+    return launch_pair<true, kBN, kPairStages, 1, kOutE4M3, false>(ma, mb, msa, msb, args, grid_sms, s, ws_bytes);
+}
+
+extern "C" int fp8_gemm_blockscaled_q8(const uint8_t* a, const float* sa, const uint8_t* b, const float* sb,
+                                       int b_scale_mode, uint8_t* q_out, float* s_out, uint32_t flags, int64_t M,
+                                       int64_t N, int64_t K, fp8_stream_t stream) {
+    return gemm_blockscaled_q8_impl(a, sa, b, sb, b_scale_mode, q_out, s_out, flags, M, N, K, nullptr, 0, stream);
+}
+
+extern "C" int fp8_gemm_blockscaled_q8_ws(const uint8_t* a, const float* sa, const uint8_t* b, const float* sb,
+                                          int b_scale_mode, uint8_t* q_out, float* s_out, uint32_t flags, int64_t M,
+                                          int64_t N, int64_t K, void* workspace, int64_t workspace_bytes,
+                                          fp8_stream_t stream) {
+    if (workspace_bytes < 0 || (workspace_bytes > 0 && !workspace)) return FP8_ERR_ARG;
+    if (workspace && !aligned16(workspace)) return FP8_ERR_ALIGN;
+    return gemm_blockscaled_q8_impl(a, sa, b, sb, b_scale_mode, q_out, s_out, flags, M, N, K,
+                                    workspace_bytes > 0 ? static_cast<float*>(workspace) : nullptr,
+                                    workspace_bytes, stream);
 }
 
 extern "C" int fp8_grouped_gemm_blockscaled(const uint8_t* a, const float* sa, const uint8_t* b, const float* sb,

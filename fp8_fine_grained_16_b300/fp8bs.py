@@ -47,8 +47,10 @@ _SIGS = {
     "fp8_quant_act_128x1": [_P, _I64, _I64, _I64, _P, _P, _U32, _P],
     "fp8_quant_weight_128x128": [_P, _I64, _I64, _I64, _P, _P, _U32, _P],
     "fp8_gemm_blockscaled": [_P, _P, _P, _P, _I, _P, _I, _I64, _I64, _I64, _P],
+    "fp8_gemm_blockscaled_ws": [_P, _P, _P, _P, _I, _P, _I, _I64, _I64, _I64, _P, _I64, _P],
     "fp8_gemm_blockscaled_pow2": [_P, _P, _P, _P, _I, _P, _I, _I64, _I64, _I64, _P],
     "fp8_gemm_blockscaled_q8": [_P, _P, _P, _P, _I, _P, _P, _U32, _I64, _I64, _I64, _P],
+    "fp8_gemm_blockscaled_q8_ws": [_P, _P, _P, _P, _I, _P, _P, _U32, _I64, _I64, _I64, _P, _I64, _P],
     "fp8_swiglu_quant_1x128": [_P, _I64, _I64, _I64, _P, _P, _U32, _P],
     "fp8_transpose_128x128": [_P, _P, _I64, _I64, _P, _P, _P],
     "fp8_grouped_gemm_blockscaled": [_P, _P, _P, _P, _P, _I, _I64, _I64, _I64, _P, _P],
@@ -66,13 +68,16 @@ for _name, _args in _SIGS.items():
     _f.restype = _I
 lib.fp8_moe_route_workspace_size.argtypes = [_I64, _I]
 lib.fp8_moe_route_workspace_size.restype = _I64
+lib.fp8_gemm_blockscaled_workspace_bytes.argtypes = [_I64, _I64, _I64]
+lib.fp8_gemm_blockscaled_workspace_bytes.restype = _I64
 lib.fp8_strerror.argtypes = [_I]
 lib.fp8_strerror.restype = ctypes.c_char_p
 lib.fp8_version.argtypes = []
 lib.fp8_version.restype = _I
 
 #: every symbol include/fp8bs.h declares
-EXPORTED = sorted(list(_SIGS) + ["fp8_moe_route_workspace_size", "fp8_strerror", "fp8_version"])
+EXPORTED = sorted(list(_SIGS) + ["fp8_moe_route_workspace_size", "fp8_gemm_blockscaled_workspace_bytes",
+                                  "fp8_strerror", "fp8_version"])
 
 
 class FP8Error(RuntimeError):
@@ -163,9 +168,32 @@ def fp8_quant_weight_128x128(w: torch.Tensor, q=None, s=None, flags: int = 0, st
 
 
 # ---------------------------------------------------------------- GEMMs
+# One split workspace per (device, stream): calls on one stream run in order,
+# so they can share it.  Its size depends only on the device, so an entry is
+# allocated once and never replaced (nothing frees memory a queued call uses).
+_GEMM_WS: dict = {}
+
+
+def _gemm_workspace(device: torch.device, stream_handle: int, M: int, N: int, K: int):
+    need = lib.fp8_gemm_blockscaled_workspace_bytes(M, N, K)
+    if need < 0:
+        _check("fp8_gemm_blockscaled_workspace_bytes", int(need))
+    if need == 0:
+        return None, 0
+    key = (device.index, stream_handle)
+    ws = _GEMM_WS.get(key)
+    if ws is None or ws.numel() < need:
+        ws = torch.empty(need, dtype=torch.uint8, device=device)
+        _GEMM_WS[key] = ws
+    return ws, need
+
+
 def fp8_gemm_blockscaled(a, sa, b, sb, b_scale_mode: int = FP8_BSCALE_BLOCK128, out_dtype=torch.bfloat16,
-                         d=None, stream=None) -> torch.Tensor:
-    """D[M, N] = block-scaled a[M, K] x b[N, K]^T (bf16 or fp32 out)."""
+                         d=None, stream=None, split: bool = True) -> torch.Tensor:
+    """D[M, N] = block-scaled a[M, K] x b[N, K]^T (bf16 or fp32 out).  With
+    ``split`` (the default) it calls fp8_gemm_blockscaled_ws with a workspace
+    kept per device and stream, so a short last wave of tiles is split along
+    K; ``split=False`` calls fp8_gemm_blockscaled."""
     M, K = a.shape
     N = b.shape[0]
     if b.shape[1] != K:
@@ -173,9 +201,15 @@ def fp8_gemm_blockscaled(a, sa, b, sb, b_scale_mode: int = FP8_BSCALE_BLOCK128, 
     d_dtype = FP8_OUT_F32 if out_dtype == torch.float32 else FP8_OUT_BF16
     if d is None:
         d = torch.empty((M, N), dtype=torch.float32 if d_dtype == FP8_OUT_F32 else torch.bfloat16, device=a.device)
-    _check("fp8_gemm_blockscaled", lib.fp8_gemm_blockscaled(
-        _ptr(a, torch.uint8, "a"), _ptr(sa, torch.float32, "sa"), _ptr(b, torch.uint8, "b"),
-        _ptr(sb, torch.float32, "sb"), b_scale_mode, _ptr(d, None, "d"), d_dtype, M, N, K, _stream(stream)))
+    args = (_ptr(a, torch.uint8, "a"), _ptr(sa, torch.float32, "sa"), _ptr(b, torch.uint8, "b"),
+            _ptr(sb, torch.float32, "sb"), b_scale_mode, _ptr(d, None, "d"), d_dtype, M, N, K)
+    st = _stream(stream)
+    if not split:
+        _check("fp8_gemm_blockscaled", lib.fp8_gemm_blockscaled(*args, st))
+        return d
+    ws, nbytes = _gemm_workspace(a.device, st, M, N, K)
+    _check("fp8_gemm_blockscaled_ws", lib.fp8_gemm_blockscaled_ws(
+        *args, None if ws is None else ws.data_ptr(), nbytes, st))
     return d
 
 
@@ -210,19 +244,27 @@ def fp8_swiglu_quant_1x128(y: torch.Tensor, I: int, q=None, s=None, flags: int =
 
 
 def fp8_gemm_blockscaled_q8(a, sa, b, sb, b_scale_mode: int = FP8_BSCALE_BLOCK128, flags: int = 0,
-                            q_out=None, s_out=None, stream=None):
+                            q_out=None, s_out=None, stream=None, split: bool = True):
     """D = block-scaled a x b^T, quantised in the epilogue per 1x128 tile along N:
-    (q u8 [M, N], s f32 [N/128, M]), the layout fp8_quant_act_1x128 produces."""
+    (q u8 [M, N], s f32 [N/128, M]), the layout fp8_quant_act_1x128 produces.
+    ``split`` as for fp8_gemm_blockscaled (fp8_gemm_blockscaled_q8_ws with the
+    per-stream workspace, or fp8_gemm_blockscaled_q8 without)."""
     M, K = a.shape
     N = b.shape[0]
     if b.shape[1] != K:
         raise ValueError("a and b disagree on K")
     q_out = torch.empty((M, N), dtype=torch.uint8, device=a.device) if q_out is None else q_out
     s_out = torch.empty((N // 128, M), dtype=torch.float32, device=a.device) if s_out is None else s_out
-    _check("fp8_gemm_blockscaled_q8", lib.fp8_gemm_blockscaled_q8(
-        _ptr(a, torch.uint8, "a"), _ptr(sa, torch.float32, "sa"), _ptr(b, torch.uint8, "b"),
-        _ptr(sb, torch.float32, "sb"), b_scale_mode, _ptr(q_out, torch.uint8, "q_out"),
-        _ptr(s_out, torch.float32, "s_out"), flags, M, N, K, _stream(stream)))
+    args = (_ptr(a, torch.uint8, "a"), _ptr(sa, torch.float32, "sa"), _ptr(b, torch.uint8, "b"),
+            _ptr(sb, torch.float32, "sb"), b_scale_mode, _ptr(q_out, torch.uint8, "q_out"),
+            _ptr(s_out, torch.float32, "s_out"), flags, M, N, K)
+    st = _stream(stream)
+    if not split:
+        _check("fp8_gemm_blockscaled_q8", lib.fp8_gemm_blockscaled_q8(*args, st))
+        return q_out, s_out
+    ws, nbytes = _gemm_workspace(a.device, st, M, N, K)
+    _check("fp8_gemm_blockscaled_q8_ws", lib.fp8_gemm_blockscaled_q8_ws(
+        *args, None if ws is None else ws.data_ptr(), nbytes, st))
     return q_out, s_out
 
 

@@ -171,6 +171,34 @@ FP8_API int fp8_gemm_blockscaled(const uint8_t* a, const float* sa,
                                  fp8_stream_t stream);
 
 /* ------------------------------------------------------------------------
+ * fp8_gemm_blockscaled with a workspace for splitting the last tiles along
+ * K.  Tiles are 256 x 256 and each pair of SMs owns whole tiles; when the
+ * tiles leave a last wave of at most half the SM pairs (or are fewer than
+ * the pairs), those tiles are computed as K ranges, one per SM pair, each
+ * range's promoted fp32 sum written to the workspace, and a second kernel
+ * on the same stream adds a tile's ranges in K order and stores D.  D is the
+ * same sum of promoted K blocks, grouped into per-range fp32 sums (the
+ * order of the fp32 additions differs from fp8_gemm_blockscaled; the result
+ * is deterministic).
+ *   workspace        device memory, 16-byte aligned, owned by the caller,
+ *                    not read before it is written; it must not be used by
+ *                    another call until this call's work on `stream` ends.
+ *                    NULL (with workspace_bytes 0): no split.
+ *   workspace_bytes  its size; fp8_gemm_blockscaled_workspace_bytes gives
+ *                    the most a call of that shape uses on the current
+ *                    device (0 when it would never split).  A smaller
+ *                    workspace disables the split where it does not fit.
+ * Other arguments, layouts and errors as fp8_gemm_blockscaled;
+ * FP8_ERR_ALIGN for a misaligned workspace, FP8_ERR_ARG for a negative size
+ * or a size without a pointer.
+ * ---------------------------------------------------------------------- */
+FP8_API int64_t fp8_gemm_blockscaled_workspace_bytes(int64_t M, int64_t N, int64_t K);
+FP8_API int fp8_gemm_blockscaled_ws(const uint8_t* a, const float* sa,
+                                    const uint8_t* b, const float* sb, int b_scale_mode,
+                                    void* d, int d_dtype, int64_t M, int64_t N, int64_t K,
+                                    void* workspace, int64_t workspace_bytes, fp8_stream_t stream);
+
+/* ------------------------------------------------------------------------
  * The block-scaled GEMM with its result quantised in the epilogue (page 2:
  * BF16 activations are read from HBM, quantised and written back, only to
  * be read again for the next MMA; quantising the producer's output where it
@@ -189,6 +217,16 @@ FP8_API int fp8_gemm_blockscaled_q8(const uint8_t* a, const float* sa,
                                     const uint8_t* b, const float* sb, int b_scale_mode,
                                     uint8_t* q_out, float* s_out, uint32_t flags,
                                     int64_t M, int64_t N, int64_t K, fp8_stream_t stream);
+
+/* fp8_gemm_blockscaled_q8 with the tail-split workspace of
+ * fp8_gemm_blockscaled_ws (same rules and sizes).  Split tiles are
+ * quantised by the fix-up kernel from the fp32 sum of their K ranges, by the
+ * same 1x128 rule. */
+FP8_API int fp8_gemm_blockscaled_q8_ws(const uint8_t* a, const float* sa,
+                                       const uint8_t* b, const float* sb, int b_scale_mode,
+                                       uint8_t* q_out, float* s_out, uint32_t flags,
+                                       int64_t M, int64_t N, int64_t K,
+                                       void* workspace, int64_t workspace_bytes, fp8_stream_t stream);
 
 /* ------------------------------------------------------------------------
  * The same GEMM for power-of-two scales (the quantisers' FP8_SCALE_POW2

@@ -86,6 +86,13 @@ def test_gemm_argument_errors(fb):
     assert call(N=200) == -2
     assert call(d=FAKE + 4) == -3
     assert call(M=0) == -1
+    w = L.fp8_gemm_blockscaled_ws
+    assert w(None, FAKE, FAKE, FAKE, 0, FAKE, 0, 128, 256, 4096, FAKE, 1 << 20, None) == -1  # null a
+    assert w(FAKE, FAKE, FAKE, FAKE, 0, FAKE, 0, 128, 256, 4096, None, 1 << 20, None) == -1  # size, no pointer
+    assert w(FAKE, FAKE, FAKE, FAKE, 0, FAKE, 0, 128, 256, 4096, FAKE, -1, None) == -1       # negative size
+    assert w(FAKE, FAKE, FAKE, FAKE, 0, FAKE, 0, 128, 256, 4096, FAKE + 8, 1 << 20, None) == -3  # misaligned
+    assert w(FAKE, FAKE, FAKE, FAKE, 0, FAKE, 0, 128, 256, 200, FAKE, 1 << 20, None) == -2   # K % 128
+    assert L.fp8_gemm_blockscaled_workspace_bytes(0, 256, 4096) == -1
     g = fb.lib.fp8_grouped_gemm_blockscaled
     assert g(FAKE, FAKE, FAKE, FAKE, FAKE, 0, 10, 256, 256, FAKE, None) == -1            # E = 0
     assert g(FAKE, FAKE, FAKE, FAKE, FAKE, 2000, 10, 256, 256, FAKE, None) == -1         # E too large
@@ -123,6 +130,10 @@ def test_pow2_and_fused_entry_point_argument_errors(fb):
     assert q(FAKE, FAKE, FAKE, FAKE, 0, FAKE, FAKE, 0, 128, 256, 100, None) == -2            # K % 128
     assert q(FAKE, FAKE, FAKE, FAKE, 0, FAKE + 8, FAKE, 0, 128, 256, 256, None) == -3        # misaligned q_out
     assert q(FAKE, FAKE, FAKE, FAKE, 0, FAKE, FAKE + 2, 0, 128, 256, 256, None) == -3        # misaligned s_out
+    qw = L.fp8_gemm_blockscaled_q8_ws
+    assert qw(FAKE, FAKE, FAKE, FAKE, 0, FAKE, FAKE, 0, 128, 256, 4096, None, 64, None) == -1    # size, no pointer
+    assert qw(FAKE, FAKE, FAKE, FAKE, 0, FAKE, FAKE, 0, 128, 256, 4096, FAKE + 4, 64, None) == -3  # misaligned
+    assert qw(FAKE, FAKE, FAKE, FAKE, 0, None, FAKE, 0, 128, 256, 4096, FAKE, 64, None) == -1    # null q_out
     # SwiGLU + quantisation
     s = L.fp8_swiglu_quant_1x128
     assert s(FAKE, 4, 128, 255, FAKE, FAKE, 1, None) == -1                                   # ldy < 2I

@@ -152,6 +152,25 @@ def test_gemm_many_tiles_per_cluster_full_rows(fb, orc, mode, out_dtype, K):
         assert n_bad == 0, "many tiles mode%d K%d rep%d: %d elements beyond the element-wise bound" % (mode, K, rep, n_bad)
 
 
+@pytest.mark.parametrize("mode", [0, 1])
+@pytest.mark.parametrize("M,N,K", [(2048, 4096, 8192), (7168, 7168, 8192)])
+def test_gemm_repeat_runs_bit_identical(fb, M, N, K, mode):
+    """The GEMM is a fixed sequence of fp32 operations, so repeated runs must
+    agree bit for bit.  Scales vary per K block (per column too in mode 1), so
+    a scale read from a stage already refilled with another K block's scales
+    changes the result; with scales all equal it would not."""
+    a, b = rand_codes((M, K), 91), rand_codes((N, K), 92)
+    sa = rand_scales((K // 128, M), 93)
+    sb = rand_scales((N // 128, K // 128) if mode == 0 else (K // 128, N), 94)
+    A, SA, B, SB = _dev(a), _dev(sa), _dev(b), _dev(sb)
+    first = fb.fp8_gemm_blockscaled(A, SA, B, SB, mode, torch.float32)
+    for rep in range(3):
+        again = fb.fp8_gemm_blockscaled(A, SA, B, SB, mode, torch.float32)
+        n_diff = int((first.view(torch.int32) != again.view(torch.int32)).sum())
+        assert n_diff == 0, "mode%d M%d N%d K%d rep%d: %d elements differ" % (mode, M, N, K, rep, n_diff)
+    assert fb.fp8_get_status() == 0
+
+
 def test_tensor_core_accumulation_precision_probe(fb, orc):
     """How many bits the tcgen05 E4M3 accumulation keeps inside one 128-element
     K block (pages 2 and 4: Hopper's limited accumulation width is why partial

@@ -49,8 +49,11 @@ def _exact_operands(M, N, K, mode, seed):
 
 @pytest.mark.parametrize("flags", [0, 1])
 @pytest.mark.parametrize("mode", [0, 1])
-@pytest.mark.parametrize("M,N,K", [(128, 256, 512), (1, 256, 128), (300, 384, 1024), (513, 768, 512)])
+@pytest.mark.parametrize("M,N,K", [(128, 256, 512), (1, 256, 128), (300, 384, 1024), (513, 768, 512),
+                                   (300, 384, 2048), (513, 768, 2048)])
 def test_q8_epilogue_bit_exact_on_exactly_representable_products(fb, orc, M, N, K, mode, flags):
+    # K >= 2048: the few tiles are split along K over the GPU and the fix-up
+    # kernel quantises them from the sum of their K ranges
     a, sa, b, sb = _exact_operands(M, N, K, mode, 7 * M + N + K + mode)
     ref = orc.gemm_blockscaled(a, sa, b, sb, mode)
     ref32 = ref.astype(np.float32)
@@ -61,6 +64,25 @@ def test_q8_epilogue_bit_exact_on_exactly_representable_products(fb, orc, M, N, 
     assert_same_bits(q, q_ref, "codes M%d N%d K%d mode%d flags%d" % (M, N, K, mode, flags))
     assert_same_bits(s, s_ref, "scales M%d N%d K%d mode%d flags%d" % (M, N, K, mode, flags))
     assert fb.fp8_get_status() == 0
+
+
+@pytest.mark.parametrize("flags", [0, 1])
+def test_q8_split_tail_bit_exact_rows(fb, orc, flags):
+    """4096 x 7168 x 2048: whole tiles quantised in the GEMM's epilogue and the
+    last wave's tiles split along K and quantised by the fix-up kernel; every
+    7th row's codes and scales against the tile rule on the exact product."""
+    M, N, K = 4096, 7168, 2048
+    a, sa, b, sb = _exact_operands(M, N, K, 0, 77 + flags)
+    rows = np.arange(0, M, 7)
+    ref = orc.gemm_blockscaled(a, sa, b, sb, 0, rows=rows, cols=np.arange(N))
+    ref32 = ref.astype(np.float32)
+    assert np.array_equal(ref32.astype(np.float64), ref), "operands were meant to give an exact fp32 product"
+    q_ref, s_ref = orc.quant_act_1x128_f32(ref32, flags)
+    q, s = fb.fp8_gemm_blockscaled_q8(_dev(a), _dev(sa), _dev(b), _dev(sb), 0, flags)
+    torch.cuda.synchronize()
+    assert fb.fp8_get_status() == 0
+    assert_same_bits(q[torch.from_numpy(rows).cuda()], q_ref, "codes flags%d" % flags)
+    assert_same_bits(s[:, torch.from_numpy(rows).cuda()].contiguous(), s_ref, "scales flags%d" % flags)
 
 
 @pytest.mark.parametrize("flags", [0, 1])
