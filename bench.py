@@ -312,7 +312,7 @@ def run_ours(args, ws, rank, local):
                 "ms_per_step": round(e2e, 4), "steps": e2e_steps,
                 "h2d_bytes_per_step": x.numel() * 2 + w.numel() * 2, "d2h_bytes_per_step": y.numel() * 2},
         # quant_act_1x128, quant_weight_128x128, the GEMM and (when it splits its last wave) its fix-up
-        "gpu_launches": (2 + gemm_launches(M, N, K, dev)) * args.steps,
+        "gpu_launches": (2 + gemm_launches(F, M, N, K, dev)) * args.steps,
         "clocks": clocks,
     }
     if rows is not None:
@@ -322,15 +322,13 @@ def run_ours(args, ws, rank, local):
     return out
 
 
-def gemm_launches(m, n, k, dev) -> int:
+def gemm_launches(F, m, n, k, dev) -> int:
     """Kernels one fp8_gemm_blockscaled call (with its workspace) launches: the
-    GEMM, plus the fix-up kernel when the library splits the last wave along K
-    (256 x 256 tiles on one SM pair each; a last wave of at most half the
-    pairs; at least 16 K blocks)."""
+    GEMM, plus the fix-up kernel when the library's plan splits the last wave
+    along K (256 x 256 tiles on one SM pair each)."""
     pairs = torch.cuda.get_device_properties(dev).multi_processor_count // 2
-    tiles = ((m + 255) // 256) * ((n + 255) // 256)
-    tail = tiles % pairs
-    return 2 if (k // 128 >= 16 and 0 < tail and 2 * tail <= pairs) else 1
+    split, _, _ = F.fp8_gemm_split_plan(m, n, k, pairs, F.lib.fp8_gemm_blockscaled_workspace_bytes(m, n, k))
+    return 2 if split > 0 else 1
 
 
 def _time(fn, reps, warm, flush, stream):

@@ -55,6 +55,7 @@
 // exit (both CTAs meet at a final cluster barrier first).
 #include "common.cuh"
 #include "expert_sched.cuh"
+#include "tail_split.cuh"
 #include "tensor_map.cuh"
 
 namespace fp8bs {
@@ -293,21 +294,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     };
     int64_t num_tiles;
     if constexpr (GROUPED) num_tiles = gs.count(); else num_tiles = ds.count();
-    // This cluster's work units: the tiles w = cluster + i * nclusters below
-    // the split tiles (whole K), then, under a tail split, K range s of split
-    // tile j, where cluster = j * split + s (its workspace slab).
-    struct Unit {
-        int64_t w, kb0, kb1;
-        int64_t slab;            // < 0: whole tile, stored to D
-    };
-    const bool splitting = !GROUPED && args.split > 0;
-    const int64_t whole_end = splitting ? args.tail0 : num_tiles;
-    const int64_t n_whole = whole_end > cluster ? (whole_end - cluster + nclusters - 1) / nclusters : 0;
-    const int64_t n_units = n_whole + ((splitting && cluster < (num_tiles - args.tail0) * args.split) ? 1 : 0);
-    auto unit_at = [&](int64_t i) -> Unit {
-        if (i < n_whole) return Unit{cluster + i * nclusters, 0, nkb, -1};
-        const int64_t j = cluster / args.split, sp = cluster % args.split;
-        return Unit{args.tail0 + j, sp * nkb / args.split, (sp + 1) * nkb / args.split, cluster};
+    // This cluster's work units (tail_split.cuh): whole tiles, then under a
+    // tail split one K range of one tail tile.
+    const int64_t split = GROUPED ? 0 : int64_t(args.split);
+    const int64_t n_units = pair_units(cluster, nclusters, num_tiles, split, args.tail0);
+    auto unit_at = [&](int64_t i) -> WorkUnit {
+        return pair_unit(i, cluster, nclusters, num_tiles, nkb, split, args.tail0);
     };
     auto sb_row = [&](const Tile& t, int h) -> int64_t {
         const int64_t c0 = int64_t(t.n0) + h * kHalf;
@@ -323,7 +315,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 uint32_t it = 0;
                 bool ok = true;
                 for (int64_t ui = 0; ok && ui < n_units; ++ui) {
-                    const Unit u = unit_at(ui);
+                    const WorkUnit u = unit_at(ui);
                     const Tile t = tile_at(u.w);
                     int64_t sbr[2] = {0, 0};
                     if constexpr (BMODE == 0) {
@@ -385,7 +377,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 uint32_t it = 0, g = 0;
                 bool ok = true;
                 for (int64_t ui = 0; ok && ui < n_units; ++ui) {
-                    const Unit u = unit_at(ui);
+                    const WorkUnit u = unit_at(ui);
                     for (int64_t kb = u.kb0; kb < u.kb1; ++kb) {
                         const uint32_t buf = g & 1u;
                         const uint32_t stage = it % STAGES, phase = (it / STAGES) & 1u;
@@ -444,7 +436,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint32_t g = 0;
         bool ok = true;
         for (int64_t ui = 0; ok && ui < n_units; ++ui) {
-            const Unit u = unit_at(ui);
+            const WorkUnit u = unit_at(ui);
             const Tile t = tile_at(u.w);
             // Where this K block's scales sit in the stage's boxes: the sA box
             // starts at (kb*M + row0) rounded down to 4 elements, the BMODE-0 sB
@@ -665,8 +657,7 @@ __global__ void __launch_bounds__(256) splitk_fixup_kernel(const float* __restri
 
 // ---------------------------------------------------------------- host side
 constexpr int kBN = 256;
-constexpr int kSplitMinKBlocks = 16;                 // below this a split saves less than the fix-up costs
-constexpr int64_t kSlabBytes = int64_t(2 * BM) * kBN * 4;
+constexpr int64_t kSlabBytes = int64_t(2 * BM) * kBN * 4;     // one pair tile of fp32 K-range sums
 
 // Workspace the tail split may use on this device: one slab per cluster.
 static int64_t split_workspace_bytes(int sms, int64_t K) {
@@ -706,27 +697,18 @@ static int launch_pair(const CUtensorMap& ma, const CUtensorMap& mb, const CUten
     if (cudaOccupancyMaxActiveClusters(&max_clusters, kern, &cfg) != cudaSuccess || max_clusters <= 0)
         return FP8_ERR_CUDA;
     int clusters = max_clusters < sms / 2 ? max_clusters : sms / 2;
-    // Tail split: a last wave of at most half the clusters is cut along K,
-    // one K range per cluster (so the slabs never exceed one per cluster).
-    // Every launched cluster gets work: when all tiles are split, exactly
-    // one cluster per K range; without a split, at most one per tile.
+    // Tail split and the number of pairs to launch (tail_split.cuh): every
+    // launched pair gets work, and the slabs never exceed one per pair.
     args.split = 0;
     int64_t num_m2 = 0, n_tail = 0;
     if constexpr (PAIR && !GROUPED) {
         num_m2 = (args.M + 2 * BM - 1) / (2 * BM);
         const int64_t num_tiles = num_m2 * ((args.N + BN - 1) / BN);
-        const int64_t nkb = args.K / BK;
-        n_tail = num_tiles % clusters;
-        if (args.ws && nkb >= kSplitMinKBlocks && n_tail > 0 && 2 * n_tail <= clusters) {
-            int64_t sp = clusters / n_tail;
-            if (sp > nkb / 2) sp = nkb / 2;
-            if (n_tail * sp * kSlabBytes <= ws_bytes) {
-                args.split = int32_t(sp);
-                args.tail0 = num_tiles - n_tail;
-                if (args.tail0 == 0) clusters = int(n_tail * sp);
-            }
-        }
-        if (args.split == 0 && num_tiles < clusters) clusters = int(num_tiles);
+        const SplitPlan plan = plan_tail_split(num_tiles, args.K / BK, clusters, args.ws ? ws_bytes / kSlabBytes : 0);
+        args.split = int32_t(plan.split);
+        args.tail0 = plan.tail0;
+        n_tail = num_tiles - plan.tail0;
+        clusters = int(plan.pairs);
     }
     cfg.gridDim = dim3(2 * clusters);
     if (cudaLaunchKernelEx(&cfg, kern, ma, mb, msa, msb, args) != cudaSuccess) return FP8_ERR_CUDA;
@@ -800,6 +782,37 @@ extern "C" int fp8_gemm_blockscaled(const uint8_t* a, const float* sa, const uin
                                     int b_scale_mode, void* d, int d_dtype, int64_t M, int64_t N, int64_t K,
                                     fp8_stream_t stream) {
     return gemm_blockscaled_impl(a, sa, b, sb, b_scale_mode, d, d_dtype, M, N, K, nullptr, 0, stream);
+}
+
+extern "C" int fp8_gemm_split_plan(int64_t M, int64_t N, int64_t K, int pairs, int64_t workspace_bytes,
+                                   int64_t* split, int64_t* tail0, int64_t* launched_pairs) {
+    if (M <= 0 || N <= 0 || K <= 0 || pairs <= 0 || workspace_bytes < 0 || !split || !tail0 || !launched_pairs)
+        return FP8_ERR_ARG;
+    if (K % 128 || N % 128) return FP8_ERR_SHAPE;
+    const int64_t num_tiles = ((M + 2 * BM - 1) / (2 * BM)) * ((N + kBN - 1) / kBN);
+    const SplitPlan p = plan_tail_split(num_tiles, K / BK, pairs, workspace_bytes / kSlabBytes);
+    *split = p.split;
+    *tail0 = p.tail0;
+    *launched_pairs = p.pairs;
+    return FP8_OK;
+}
+
+extern "C" int64_t fp8_gemm_split_units(int64_t M, int64_t N, int64_t K, int pairs, int64_t workspace_bytes,
+                                        int64_t pair, int64_t* units, int64_t max_units) {
+    int64_t split, tail0, np;
+    const int rc = fp8_gemm_split_plan(M, N, K, pairs, workspace_bytes, &split, &tail0, &np);
+    if (rc != FP8_OK) return rc;
+    if (pair < 0 || pair >= np || max_units < 0 || (max_units > 0 && !units)) return FP8_ERR_ARG;
+    const int64_t num_tiles = ((M + 2 * BM - 1) / (2 * BM)) * ((N + kBN - 1) / kBN);
+    const int64_t n = pair_units(pair, np, num_tiles, split, tail0);
+    for (int64_t i = 0; i < n && i < max_units; ++i) {
+        const WorkUnit u = pair_unit(i, pair, np, num_tiles, K / BK, split, tail0);
+        units[4 * i] = u.w;
+        units[4 * i + 1] = u.kb0;
+        units[4 * i + 2] = u.kb1;
+        units[4 * i + 3] = u.slab;
+    }
+    return n;
 }
 
 extern "C" int64_t fp8_gemm_blockscaled_workspace_bytes(int64_t M, int64_t N, int64_t K) {
