@@ -151,8 +151,9 @@ class Clocks:
                           ("swt", "sw_thermal_slowdown"), ("cap", "sw_power_cap")):
             if any(r[key] for r in rows):
                 reasons.append(name)
-        return dict(sm_mhz=statistics.median(r["sm"] for r in rows), sm_max_mhz=max(r["smax"] for r in rows),
-                    reasons=reasons, samples=len(rows), power_w_max=max(r["power"] for r in rows))
+        return dict(sm_mhz=statistics.median(r["sm"] for r in rows), sm_mhz_min=min(r["sm"] for r in rows),
+                    sm_max_mhz=max(r["smax"] for r in rows), reasons=reasons, samples=len(rows),
+                    power_w_max=max(r["power"] for r in rows))
 
 
 class L2Flush:
@@ -171,7 +172,7 @@ class L2Flush:
 
 def kernel_source_sha():
     h = hashlib.sha256()
-    for f in ("gemm.cu", "common.cuh"):
+    for f in ("gemm.cu", "common.cuh", "tail_split.cuh", "expert_sched.cuh", "tensor_map.cuh"):
         h.update(open(os.path.join(ROOT, "fp8_fine_grained_16_b300", "csrc", f), "rb").read())
     return h.hexdigest()[:16]
 
@@ -277,12 +278,15 @@ def run_ours(args, ws, rank, local):
             e2e_ms.append(e_start.elapsed_time(e_end))
     e2e = sum(e2e_ms) / len(e2e_ms)
 
-    if args.rows == "all":
-        rows = measure_rows(F, S, dev, flush, pk)
-    elif args.rows == "none":
-        rows = None
-    else:
-        rows = measure_rows(F, S, dev, flush, pk, tuple(x for x in args.rows.split(",") if x))
+    rows = rows_clocks = None
+    if args.rows != "none":
+        sections = None if args.rows == "all" else tuple(x for x in args.rows.split(",") if x)
+        # clocks sampled over the whole row measurement, so that a row run at a
+        # lower SM clock shows (the step's own clocks are in "clocks")
+        with Clocks(local) as clk_rows:
+            rows = measure_rows(F, S, dev, flush, pk) if sections is None else \
+                measure_rows(F, S, dev, flush, pk, sections)
+        rows_clocks = clk_rows.summary()
 
     out = {
         "metric": METRIC,
@@ -317,6 +321,7 @@ def run_ours(args, ws, rank, local):
     }
     if rows is not None:
         out["rows"] = rows
+        out["rows_clocks"] = rows_clocks
     if rank == 0 and ws == 1 and not args.no_cpu_baseline:
         out["cpu_baseline"] = cpu_baseline(S, d=d)
     return out
