@@ -22,12 +22,14 @@
 
 namespace fp8bs {
 
-// e^x of two values for the fp32 SwiGLU above, with two-lane packed fp32
-// operations (each lane is the same IEEE operation as its scalar form).
-// x > 88 gives +inf and x < -87 gives 0: only 1 + e^x is formed, where both
-// are exact.  In-range inputs take the steps unchanged; out-of-range ones are
-// clamped for the arithmetic and replaced at the end.
-FP8_DEV float2 exp2_cody_waite(float2 x) {
+// d = 1 + e^x of two values, for sigma = 1/d in the fp32 SwiGLU above, with
+// two-lane packed fp32 operations (each lane is the same IEEE operation as
+// its scalar form).  The definition takes e^x = +inf above 88 and 0 below
+// -87.  Inputs in [-87, 88] take the steps unchanged.  An input below -87 is
+// computed at -87: e^-87 ~ 1.6e-38 is far below half an ulp of 1, so 1 + e
+// rounds to exactly 1, the d that e = 0 gives, and no select is needed for
+// it.  An input above 88 is computed at 88 and its e replaced by +inf.
+FP8_DEV float2 one_plus_exp(float2 x) {
     const float2 xc = make_float2(fminf(fmaxf(x.x, -87.0f), 88.0f), fminf(fmaxf(x.y, -87.0f), 88.0f));
     const float2 t = __fmul2_rn(xc, make_float2(0x1.715476p+0f, 0x1.715476p+0f));   // x * log2(e)
     // t to the nearest integer (ties to even, as rint): adding 1.5 * 2^23 leaves
@@ -51,13 +53,13 @@ FP8_DEV float2 exp2_cody_waite(float2 x) {
     const float2 e = __fmul2_rn(p, make_float2(__int_as_float((nx + 127) << 23),       // 2^n, n in [-126, 127]
                                                 __int_as_float((ny + 127) << 23)));
     const float inf = __int_as_float(0x7F800000);
-    return make_float2(x.x > 88.0f ? inf : (x.x < -87.0f ? 0.0f : e.x), x.y > 88.0f ? inf : (x.y < -87.0f ? 0.0f : e.y));
+    return __fadd2_rn(make_float2(1.0f, 1.0f), make_float2(x.x > 88.0f ? inf : e.x, x.y > 88.0f ? inf : e.y));
 }
 
 // (g * sigma(g)) * u for two elements, sigma(g) = 1 / (1 + e^-g); the
 // reciprocal is the correctly rounded one, equal to the IEEE quotient.
 FP8_DEV float2 swiglu2_fp32(float2 g, float2 u) {
-    const float2 d = __fadd2_rn(make_float2(1.0f, 1.0f), exp2_cody_waite(make_float2(-g.x, -g.y)));
+    const float2 d = one_plus_exp(make_float2(-g.x, -g.y));
     const float2 sig = make_float2(__frcp_rn(d.x), __frcp_rn(d.y));
     return __fmul2_rn(__fmul2_rn(g, sig), u);
 }
