@@ -9,14 +9,14 @@
 // B = W^T from this copy.
 //
 // One CTA (256 threads) per 128x128 byte tile.  Thread (warp w, lane l)
-// loads the 32-bit words at byte column 4l of the input rows 4q .. 4q+3
-// (q = w + 8j, j < 4): every load instruction of a warp reads whole 128-byte
-// rows.  Each 4x4 byte block is transposed in registers (byte permutes) and
-// lands in a shared tile whose word index is rotated per output row c by
-// (c/4 + 4*(c%4)) mod 32, which keeps both the stores (a warp writes rows
-// c = 4*lane + i) and the loads (a warp reads 16 consecutive rows, two
-// threads per row) on 32 distinct banks; the output leaves as 16-byte pieces
-// of whole 128-byte rows.
+// loads the 16-byte pieces at byte column 16s of the input rows 4q .. 4q+3
+// (s = l % 8, q = 4w + l / 8): every load instruction of a warp reads four
+// whole 128-byte rows.  Each of its four 4x4 byte blocks is transposed in
+// registers (byte permutes) and lands in a shared tile whose word index is
+// rotated per output row c by (c/4 + 4*(c%4)) mod 32, which keeps both the
+// stores (slot q + 4s + const: 32 distinct banks per warp) and the loads (a
+// warp reads 16 consecutive rows, two threads per row) conflict-free; the
+// output leaves as 16-byte pieces of whole 128-byte rows.
 #include "common.cuh"
 
 namespace fp8bs {
@@ -46,18 +46,22 @@ __global__ void __launch_bounds__(256) transpose_128x128_kernel(const uint8_t* _
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const uint8_t* src = q + (nb * 128) * K + kb * 128;
 
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-        const int qd = warp + 8 * j;                       // input row quad: rows 4qd .. 4qd+3
-        uint32_t in[4], out[4];
+    {
+        const int sg = lane & 7, qd = 4 * warp + (lane >> 3);    // 16-byte column piece, input row quad
+        uint4 in4[4];
 #pragma unroll
         for (int r = 0; r < 4; ++r)
-            in[r] = __ldg(reinterpret_cast<const uint32_t*>(src + (4 * qd + r) * K) + lane);
-        transpose4x4(in, out);
+            in4[r] = __ldg(reinterpret_cast<const uint4*>(src + (4 * qd + r) * K) + sg);
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            const int c = 4 * lane + i;                    // input column = output row
-            T[c * 32 + ((qd + lane + 4 * i) & 31)] = out[i];   // c/4 = lane, c%4 = i
+        for (int w = 0; w < 4; ++w) {
+            const uint32_t in[4] = {(&in4[0].x)[w], (&in4[1].x)[w], (&in4[2].x)[w], (&in4[3].x)[w]};
+            uint32_t out[4];
+            transpose4x4(in, out);
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const int c = 16 * sg + 4 * w + i;         // input column = output row: c/4 = 4sg + w, c%4 = i
+                T[c * 32 + ((qd + 4 * sg + w + 4 * i) & 31)] = out[i];
+            }
         }
     }
     __syncthreads();
