@@ -18,11 +18,14 @@
 // half of the B tile in its own shared memory, and each CTA's TMEM receives
 // its 128 rows of D.  Per K block a CTA moves 32 KB of operands through
 // shared memory for 128 x 256 x 128 multiply-adds (a one-CTA 128 x 256 tile
-// moves 48 KB for the same work).  Roles, per CTA:
+// moves 48 KB for the same work).  The grouped (MoE) form runs the same code
+// with one CTA per 128 x 256 tile (PAIR = false, tcgen05.mma.cta_group::1,
+// a 4-stage ring): experts hold ~128 rows each, so a 256-row pair tile would
+// spend half its MMAs on padding.  Roles, per CTA:
 //
 //   warp 0        TMA producer: A and B halves (128-byte swizzle) and the
 //                 scales the promotion needs (sA of the CTA's 128 rows, sB of
-//                 the tile's columns) into a 6-stage ring.
+//                 the tile's columns) into a 6-stage ring (4 alone).
 //   warp 1        allocates the pair's TMEM (two 256-column fp32
 //                 accumulators); in the leader CTA it issues four MMAs
 //                 (K = 32 each) per K block and commits them to both CTAs'
