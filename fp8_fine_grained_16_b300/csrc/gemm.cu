@@ -672,12 +672,8 @@ static int launch_pair(const CUtensorMap& ma, const CUtensorMap& mb, const CUten
                        GemmArgs args, int sms, cudaStream_t stream, int64_t ws_bytes = 0) {
     using L = PairLayout<PAIR, BN, STAGES, BMODE, GROUPED>;
     auto kern = gemm_pair_kernel<PAIR, BN, STAGES, BMODE, OUT, GROUPED>;
-    static bool attr_set = false;
-    if (!attr_set) {
-        if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kDynSmem) != cudaSuccess)
-            return FP8_ERR_CUDA;
-        attr_set = true;
-    }
+    static unsigned char smem_opted_in[kMaxDevices] = {};
+    if (!opt_in_dynamic_smem(kern, L::kDynSmem, smem_opted_in)) return FP8_ERR_CUDA;
     cudaLaunchConfig_t cfg = {};
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeClusterDimension;

@@ -502,12 +502,8 @@ static int launch(const CUtensorMap& ma, const CUtensorMap& mb, const Args& args
     constexpr int S = PAIR ? kStages : kSingleStages;
     using Lay = Layout<PAIR, S, GROUPED>;
     auto kern = gemm_mx_pair_kernel<PAIR, S, BMODE, OUT_F32, GROUPED>;
-    static bool attr_set = false;
-    if (!attr_set) {
-        if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Lay::kDynSmem) != cudaSuccess)
-            return FP8_ERR_CUDA;
-        attr_set = true;
-    }
+    static unsigned char smem_opted_in[kMaxDevices] = {};
+    if (!opt_in_dynamic_smem(kern, Lay::kDynSmem, smem_opted_in)) return FP8_ERR_CUDA;
     cudaLaunchConfig_t cfg = {};
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeClusterDimension;

@@ -53,6 +53,20 @@ inline bool make_scale_map(CUtensorMap* map, const float* base, int64_t n, int b
     return r == CUDA_SUCCESS;
 }
 
+// Opt `kern` into `bytes` of dynamic shared memory (above the 48 KB default)
+// on the current device, once per device: the attribute belongs to the
+// device's context, so a process that drives several GPUs sets it on each.
+constexpr int kMaxDevices = 64;
+template <typename Kern>
+inline bool opt_in_dynamic_smem(Kern kern, int bytes, unsigned char (&done)[kMaxDevices]) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return false;
+    if (done[dev]) return true;
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes) != cudaSuccess) return false;
+    done[dev] = 1;
+    return true;
+}
+
 inline int device_sms() {
     int dev = 0, n = 0, major = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return -1;
