@@ -62,3 +62,28 @@ def test_reference_arm_runs_on_rank_zero_only():
     class A:
         steps, warmup = 1, 0
     assert bench.run_reference(A, 2, 1) is None          # rank 1: no work, nothing printed
+
+
+def test_reference_arm_line_has_the_contract_keys():
+    """One step of the oracle reference arm (on this CPU): the JSON line the
+    driver reads carries the base keys, a cpu_baseline describing the run and
+    an e2e block with no host-device bytes."""
+    import json
+    import sys
+    sys.path.insert(0, ROOT)
+    import bench
+
+    class A:
+        steps, warmup = 1, 0
+    out = bench.run_reference(A, 1, 0)
+    json.dumps(out)                                       # serialisable as one line
+    for k in ("impl", "metric", "value", "unit", "n_gpus", "steps", "warmup", "ms_per_step",
+              "higher_is_better", "scaling", "vs_baseline", "dtype", "data", "config", "cpu_baseline", "e2e"):
+        assert k in out, k
+    assert out["impl"] == "reference" and out["metric"] == bench.METRIC and out["unit"] == "TFLOP/s"
+    assert out["value"] > 0 and out["higher_is_better"] is True and out["n_gpus"] == 1
+    cb = out["cpu_baseline"]
+    assert cb["kind"] == "oracle" and cb["cores"] >= 1 and cb["sample"] and cb["value"] == out["value"]
+    e2e = out["e2e"]
+    assert e2e["value"] == out["value"] and e2e["unit"] == out["unit"]
+    assert e2e["h2d_bytes_per_step"] == 0 and e2e["d2h_bytes_per_step"] == 0
