@@ -65,9 +65,9 @@ def test_reference_arm_runs_on_rank_zero_only():
 
 
 def test_reference_arm_line_has_the_contract_keys():
-    """One step of the oracle reference arm (on this CPU): the JSON line the
-    driver reads carries the base keys, a cpu_baseline describing the run and
-    an e2e block with no host-device bytes."""
+    """One step of the oracle reference arm (on this CPU): the JSON line it
+    prints carries the base keys, a cpu_baseline describing the run and an
+    e2e block with no host-device bytes."""
     import json
     import sys
     sys.path.insert(0, ROOT)
