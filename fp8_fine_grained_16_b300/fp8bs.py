@@ -192,6 +192,18 @@ def _gemm_workspace(device: torch.device, stream_handle: int, M: int, N: int, K:
     return ws, need
 
 
+def release_gemm_workspaces() -> int:
+    """Free the split workspaces kept per device and stream (one slab per SM
+    pair, 18.9 MB on a 148-SM GPU, per stream that ran a split GEMM).  It
+    waits for the GPU first, so no queued GEMM still uses them.  Returns how
+    many were freed; later calls allocate again as needed."""
+    n = len(_GEMM_WS)
+    if n:
+        torch.cuda.synchronize()
+        _GEMM_WS.clear()
+    return n
+
+
 def fp8_gemm_split_plan(M: int, N: int, K: int, pairs: int, workspace_bytes: int):
     """(split, tail0, launched_pairs) of the dense GEMM's tail split (host only)."""
     out = (ctypes.c_int64 * 3)()

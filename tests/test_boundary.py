@@ -147,3 +147,7 @@ def test_pow2_and_fused_entry_point_argument_errors(fb):
     assert t(FAKE + 4, FAKE, 128, 128, FAKE, FAKE, None) == -3                               # misaligned q
     assert t(None, FAKE, 128, 128, FAKE, FAKE, None) == -1
     assert "power of two" in fb.fp8_strerror(fb.FP8_ERR_SCALE)
+
+
+def test_releasing_no_gemm_workspaces_needs_no_gpu(fb):
+    assert fb.release_gemm_workspaces() == 0

@@ -108,3 +108,15 @@ def test_small_problems_split_over_the_gpu(fb, orc, M, N, K, mode, out_dtype):
     got = to_np(d1)
     assert_gemm_close(got, ref, bf16, orc, "split M%d N%d K%d mode%d" % (M, N, K, mode))
     assert _elementwise_ok(got, ref, bf16) == 0
+
+
+def test_released_workspaces_are_allocated_again(fb):
+    a, sa, b, sb = _operands(256, 256, 2048, 0, 3)
+    A, SA, B, SB = _dev(a), _dev(sa), _dev(b), _dev(sb)
+    d1 = fb.fp8_gemm_blockscaled(A, SA, B, SB, 0, torch.float32)
+    assert fb.release_gemm_workspaces() >= 1
+    assert fb.release_gemm_workspaces() == 0
+    d2 = fb.fp8_gemm_blockscaled(A, SA, B, SB, 0, torch.float32)
+    torch.cuda.synchronize()
+    assert torch.equal(d1.view(torch.int32), d2.view(torch.int32))
+    assert fb.fp8_get_status() == 0
