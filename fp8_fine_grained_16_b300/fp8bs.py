@@ -192,14 +192,22 @@ def _gemm_workspace(device: torch.device, stream_handle: int, M: int, N: int, K:
     return ws, need
 
 
-def release_gemm_workspaces() -> int:
+def _workspace_devices() -> list:
+    """The device indices that hold a split workspace (each must be waited
+    for before its workspace goes back to the caching allocator)."""
+    return sorted({dev for dev, _ in _GEMM_WS})
+
+
+def release_gemm_workspaces(_synchronize=torch.cuda.synchronize) -> int:
     """Free the split workspaces kept per device and stream (one slab per SM
     pair, 18.9 MB on a 148-SM GPU, per stream that ran a split GEMM).  It
-    waits for the GPU first, so no queued GEMM still uses them.  Returns how
-    many were freed; later calls allocate again as needed."""
+    first waits for every device that holds one, so no GEMM queued on any
+    of them still reads or writes its workspace.  Returns how many were
+    freed; later calls allocate again as needed."""
     n = len(_GEMM_WS)
     if n:
-        torch.cuda.synchronize()
+        for dev in _workspace_devices():
+            _synchronize(dev)
         _GEMM_WS.clear()
     return n
 

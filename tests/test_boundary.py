@@ -151,3 +151,21 @@ def test_pow2_and_fused_entry_point_argument_errors(fb):
 
 def test_releasing_no_gemm_workspaces_needs_no_gpu(fb):
     assert fb.release_gemm_workspaces() == 0
+
+
+def test_releasing_workspaces_waits_for_every_device_that_holds_one(fb):
+    """The split workspaces are keyed by (device, stream); before any goes
+    back to the caching allocator, every device holding one is waited for,
+    not only the current device (a GEMM queued on another GPU may still use
+    its workspace)."""
+    synced = []
+    saved = dict(fb._GEMM_WS)
+    fb._GEMM_WS.clear()
+    try:
+        fb._GEMM_WS.update({(0, 11): "ws0", (3, 12): "ws3a", (3, 15): "ws3b", (6, 0): "ws6"})
+        assert fb.release_gemm_workspaces(_synchronize=synced.append) == 4
+        assert synced == [0, 3, 6]
+        assert not fb._GEMM_WS
+    finally:
+        fb._GEMM_WS.clear()
+        fb._GEMM_WS.update(saved)

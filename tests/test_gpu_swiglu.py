@@ -1,15 +1,23 @@
 """GPU parity of SwiGLU fused with 1x128 quantisation (the MoE down-projection
-input; page 2: its scaling factors are integral powers of 2) against the
-oracle: codes and scales bit for bit.  Both sides form h = SiLU(g) * u in the
-same fp32 steps (e^x by Cody-Waite reduction and a degree-7 Taylor
-polynomial, written separately on each side), then apply the 1x128 tile rule.
+input; the DeepSeek-V3 FP8 training pages fix its scaling factors to
+integral powers of 2).
+
+Two checks.  The independent one holds the GPU's codes and scales to the
+plain definition: h = g / (1 + e^-g) * u in float64 with libm's exp, rounded
+once to fp32, then the oracle's pinned fp32 1x128 tile rule; they must match
+bit for bit except neighbouring codes (or powers of two) where h sits within
+the fp32 slack of a rounding midpoint (or scale boundary), and those must be
+few.  The consistency check holds them bit for bit to the oracle's fused
+quantiser, which forms h in the same fp32 steps as the kernel (e^x by
+Cody-Waite reduction and a degree-7 Taylor polynomial, written separately on
+each side).
 """
 import numpy as np
 import pytest
 import torch
 
 from fp8_fine_grained_16_b300 import synthetic as S
-from _checks import assert_same_bits
+from _checks import assert_same_bits, check_swiglu_quant_against_fp64
 
 pytestmark = pytest.mark.gpu
 
@@ -69,3 +77,39 @@ def test_swiglu_quant_moe_down_full_size_sampled(fb, orc):
     q_ref, s_ref = orc.swiglu_quant_1x128(S.bf16_bits(y[torch.from_numpy(rows)]), 2048, 1)
     assert_same_bits(q[torch.from_numpy(rows).cuda()], q_ref, "full-size codes")
     assert_same_bits(s[:, torch.from_numpy(rows).cuda()].contiguous(), s_ref, "full-size scales")
+
+
+@pytest.mark.parametrize("flags", [1, 0])
+@pytest.mark.parametrize("R,I,pad,scale", [(300, 2048, 0, 3.0), (33, 640, 24, 1.0), (2048, 1024, 8, 8.0)])
+def test_swiglu_quant_against_fp64_definition(fb, orc, R, I, pad, scale, flags):
+    y = _bf16((R, 2 * I + pad), 7 * R + I + pad, scale)
+    q, s = fb.fp8_swiglu_quant_1x128(y.cuda(), I, flags=flags)
+    torch.cuda.synchronize()
+    n_mid, n_scale = check_swiglu_quant_against_fp64(q.cpu().numpy(), s.cpu().numpy(), y, I, flags, orc)
+    print("R%d I%d flags%d: %d codes at a midpoint of %d, %d of %d tiles with another scale"
+          % (R, I, flags, n_mid, q.numel(), n_scale, s.numel()))
+    assert n_mid <= 1e-4 * q.numel() + 2
+    if flags & 1:
+        assert n_scale <= 1e-3 * s.numel() + 1
+
+
+def test_swiglu_quant_extremes_against_fp64_definition(fb, orc):
+    """Saturated and vanishing gates, zero tiles and outliers against the
+    float64 definition (pow-2 and default)."""
+    R, I = 64, 256
+    y = _bf16((R, 2 * I), 9, 1.0).float()
+    y[0, :I] = 100.0
+    y[1, :I] = -100.0
+    y[2, :I] = 1e-30
+    y[3, :] = 0.0
+    y[4, 5] = 60.0
+    y[5, I + 7] = -3e4
+    y[6, :I] = torch.linspace(-95.0, 95.0, I)
+    y = y.to(torch.bfloat16)
+    for flags in (1, 0):
+        q, s = fb.fp8_swiglu_quant_1x128(y.cuda(), I, flags=flags)
+        torch.cuda.synchronize()
+        n_mid, n_scale = check_swiglu_quant_against_fp64(q.cpu().numpy(), s.cpu().numpy(), y, I, flags, orc)
+        assert n_mid <= 2
+        if flags & 1:
+            assert n_scale <= 1

@@ -197,3 +197,68 @@ def test_f32_tile_quant_follows_the_tile_rule(orc, flags):
     err = np.abs(deq - x.astype(np.float64))
     bound = 2.0 ** -4 * np.abs(x.astype(np.float64)) * (1 + 1e-6) + 2.0 ** -10 * st
     assert np.all(err <= bound)
+
+
+def _dequant_bound(x, deq, sc):
+    err = np.abs(x - deq)
+    bound = np.maximum(np.abs(x) * 2.0 ** -4, sc * 2.0 ** -10) + np.abs(x) * 2.0 ** -20
+    return err <= bound
+
+
+@pytest.mark.parametrize("pow2", [False, True])
+def test_weight_dequant_error_bound_every_element(orc, pow2):
+    """Every code of the 128x128 quantiser dequantises within half an E4M3
+    step with its own block's scale.  The 3 x 2 blocks differ in magnitude by
+    up to 10^10, so a code formed with another block's reciprocal (a
+    transposed or shifted block index) breaks the bound by orders of
+    magnitude; one block is all zero, one holds a lone outlier."""
+    g = torch.Generator().manual_seed(17)
+    w = torch.randn((384, 256), generator=g)
+    mags = [[1e-6, 3e2], [0.02, 0.0], [7.0, 1e4]]
+    for nb in range(3):
+        for kb in range(2):
+            w[nb * 128:(nb + 1) * 128, kb * 128:(kb + 1) * 128] *= mags[nb][kb]
+    w[200, 30] = 55.0                          # outlier in block (1, 0)
+    wb = w.to(torch.bfloat16)
+    q, s = orc.quant_weight_128x128(_bits(wb), flags=int(pow2))
+    x = wb.double().numpy()
+    sc = np.repeat(np.repeat(s.astype(np.float64), 128, axis=0), 128, axis=1)
+    assert np.all(_dequant_bound(x, _decode(orc, q) * sc, sc))
+    # each block's own amax codes to +-448 in default mode (and only there)
+    if not pow2:
+        for nb in range(3):
+            for kb in range(2):
+                blk = x[nb * 128:(nb + 1) * 128, kb * 128:(kb + 1) * 128]
+                if np.abs(blk).max() == 0:
+                    # zeros keep their sign: +0 -> 0x00, -0 -> 0x80
+                    assert np.all((q[nb * 128:(nb + 1) * 128, kb * 128:(kb + 1) * 128] & 0x7F) == 0)
+                    continue
+                i, j = np.unravel_index(np.argmax(np.abs(blk)), blk.shape)
+                assert q[nb * 128 + i, kb * 128 + j] in (0x7E, 0xFE)
+
+
+@pytest.mark.parametrize("pow2", [False, True])
+def test_128x1_dequant_error_bound_every_element(orc, pow2):
+    """The same bound for the token-direction quantiser, which writes its
+    codes transposed: qT[h, t] dequantised with s[t / 128, h] must be within
+    half an E4M3 step of x[t, h].  Columns and token blocks differ in
+    magnitude (a code scaled by a neighbouring column's or token block's
+    scale breaks the bound), and one column is zero in one token block."""
+    g = torch.Generator().manual_seed(23)
+    T, H = 384, 96
+    x = torch.randn((T, H), generator=g)
+    x *= torch.logspace(-4, 4, H).reshape(1, H)
+    x *= torch.tensor([1.0, 1e-5, 3e3]).repeat_interleave(128).reshape(T, 1)
+    x[128:256, 40] = 0.0
+    xb = x.to(torch.bfloat16)
+    qT, s = orc.quant_act_128x1(_bits(xb), flags=int(pow2))
+    xv = xb.double().numpy()
+    sc = np.repeat(s.astype(np.float64), 128, axis=0)          # [T, H]: the scale of each element's tile
+    deq = _decode(orc, qT).T * sc
+    assert np.all(_dequant_bound(xv, deq, sc))
+    if not pow2:
+        for tb in range(3):
+            blk = np.abs(xv[tb * 128:(tb + 1) * 128])
+            for h in range(H):
+                if blk[:, h].max() > 0:
+                    assert qT[h, tb * 128 + int(np.argmax(blk[:, h]))] in (0x7E, 0xFE)

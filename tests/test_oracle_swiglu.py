@@ -83,3 +83,21 @@ def test_swiglu_quant_is_tile_rule_of_swiglu(orc, flags):
     q2, s2 = orc.quant_act_1x128_f32(orc.swiglu_f32(yb, I), flags)
     assert np.array_equal(q, q2)
     assert np.array_equal(s.view(np.uint32), s2.view(np.uint32))
+
+
+@pytest.mark.parametrize("flags", [1, 0])
+def test_fused_quant_against_fp64_definition(orc, flags):
+    """The oracle's fused SwiGLU quantiser (its own fp32 e^x recipe) held to
+    the float64 definition with libm's exp followed by the pinned fp32 tile
+    rule: equal codes and scales except neighbours at a rounding midpoint or
+    a scale boundary, and those few."""
+    import torch
+    from _checks import check_swiglu_quant_against_fp64
+    from fp8_fine_grained_16_b300 import synthetic as S
+    y = (torch.randn((256, 2 * 1024), generator=torch.Generator().manual_seed(31)) * 3.0).to(torch.bfloat16)
+    q, s = orc.swiglu_quant_1x128(S.bf16_bits(y), 1024, flags)
+    n_mid, n_scale = check_swiglu_quant_against_fp64(q, s, y, 1024, flags, orc)
+    print("flags%d: %d codes at a midpoint, %d tiles with another scale" % (flags, n_mid, n_scale))
+    assert n_mid <= 1e-4 * q.size + 2
+    if flags & 1:
+        assert n_scale <= 2
