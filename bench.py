@@ -336,7 +336,7 @@ def run_ours(args, ws, rank, local):
 def gemm_launches(F, m, n, k, dev) -> int:
     """Kernels one fp8_gemm_blockscaled call (with its workspace) launches: the
     GEMM, plus the fix-up kernel when the library's plan splits the last wave
-    along K (256 x 256 tiles on one SM pair each)."""
+    along K (256-row tiles on one SM pair each)."""
     pairs = torch.cuda.get_device_properties(dev).multi_processor_count // 2
     split, _, _ = F.fp8_gemm_split_plan(m, n, k, pairs, F.lib.fp8_gemm_blockscaled_workspace_bytes(m, n, k))
     return 2 if split > 0 else 1
@@ -374,6 +374,18 @@ def measure_rows(F, S, dev, flush, pk, sections=ROW_SECTIONS):
                          algorithmic_bytes=int(nbytes), peak=pk["hbm"], frac=round(gbs / pk["hbm"], 4),
                          frac_of_nominal_8000=round(gbs / HBM_NOMINAL_GBS, 4))
 
+    def grouped_row(name, ms, flop, moved, wbytes, workload):
+        """A grouped GEMM streams every expert's weights once: HBM-bound (AI ~
+        2 x rows per expert FLOP/B, below the ridge), so the row's bound and
+        fraction are HBM's; the tensor-peak fraction is kept beside them."""
+        gbs = moved / (ms * 1e-3) / 1e9
+        tf = flop / (ms * 1e-3) / 1e12
+        out[name] = dict(workload=workload, ms=round(ms, 5), bound="hbm", achieved=round(gbs, 1), unit="GB/s",
+                         algorithmic_bytes=int(moved), weight_bytes=int(wbytes), peak=pk["hbm"],
+                         frac=round(gbs / pk["hbm"], 4), frac_of_nominal_8000=round(gbs / HBM_NOMINAL_GBS, 4),
+                         tflops=round(tf, 1), tensor_frac=round(tf / fp8_peak, 4),
+                         tensor_frac_of_nominal_4500=round(tf / FP8_NOMINAL_TFLOPS, 4))
+
     def tensor_row(name, ms, flop, workload, extra=None):
         tf = flop / (ms * 1e-3) / 1e12
         r = dict(workload=workload, ms=round(ms, 5), bound="tensor", achieved=round(tf, 1), unit="TFLOP/s",
@@ -388,9 +400,9 @@ def measure_rows(F, S, dev, flush, pk, sections=ROW_SECTIONS):
     if "wgrad" in sections:
         measure_wgrad_rows(F, S, dev, flush, st, reps, warm, hbm_row, tensor_row, out)
     if "moe_up" in sections:
-        measure_moe_up_rows(F, S, dev, flush, st, reps, warm, hbm_row, tensor_row, out, pk)
+        measure_moe_up_rows(F, S, dev, flush, st, reps, warm, hbm_row, grouped_row, out)
     if "moe_down" in sections:
-        measure_moe_down_rows(F, S, dev, flush, st, reps, warm, hbm_row, tensor_row, out, pk)
+        measure_moe_down_rows(F, S, dev, flush, st, reps, warm, hbm_row, grouped_row, out)
     if "swiglu" in sections:
         measure_swiglu_rows(F, dev, flush, st, reps, warm, hbm_row)
     torch.cuda.synchronize()
@@ -459,7 +471,7 @@ def measure_wgrad_rows(F, S, dev, flush, st, reps, warm, hbm_row, tensor_row, ou
     del dy, xx, qa, qb, dw, qa2, qb2
 
 
-def measure_moe_up_rows(F, S, dev, flush, st, reps, warm, hbm_row, tensor_row, out, pk):
+def measure_moe_up_rows(F, S, dev, flush, st, reps, warm, hbm_row, grouped_row, out):
     E, k, K = 256, 8, 7168
     mu = S.moe_up(with_weights=False)
     x, logits = mu["x"].to(dev), mu["logits"].to(dev)
@@ -484,20 +496,16 @@ def measure_moe_up_rows(F, S, dev, flush, st, reps, warm, hbm_row, tensor_row, o
     ms = _time(lambda: F.fp8_grouped_gemm_blockscaled(qa, sa, qwu, swu, r["off"], d=yu), reps, warm, flush, st)
     wbytes = E * Nu * K
     moved = wbytes + R * K + R * Nu * 2
-    tensor_row("a6_grouped_moe_up", ms, 2.0 * R * Nu * K, "32768 rows, 256 experts, N=4096, K=7168",
-               dict(weight_bytes=wbytes, hbm_achieved_gbs=round(moved / (ms * 1e-3) / 1e9, 1),
-                    hbm_frac=round(moved / (ms * 1e-3) / 1e9 / pk["hbm"], 4)))
+    grouped_row("a6_grouped_moe_up", ms, 2.0 * R * Nu * K, moved, wbytes, "32768 rows, 256 experts, N=4096, K=7168")
     qx2, sx2 = F.fp8_quant_act_1x128(x, flags=P)
     qa2, sa2 = F.fp8_permute_rows(qx2, sx2, r["src_row"])
     ms = _time(lambda: F.fp8_grouped_gemm_blockscaled_pow2(qa2, sa2, qwu2, swu2, r["off"], d=yu), reps, warm, flush, st)
-    tensor_row("f1_grouped_moe_up_pow2", ms, 2.0 * R * Nu * K,
-               "32768 rows, 256 experts, N=4096, K=7168, pow-2 scales (microscaled MMA)",
-               dict(weight_bytes=wbytes, hbm_achieved_gbs=round(moved / (ms * 1e-3) / 1e9, 1),
-                    hbm_frac=round(moved / (ms * 1e-3) / 1e9 / pk["hbm"], 4)))
+    grouped_row("f1_grouped_moe_up_pow2", ms, 2.0 * R * Nu * K, moved, wbytes,
+                "32768 rows, 256 experts, N=4096, K=7168, pow-2 scales (microscaled MMA)")
     del qwu, qwu2, yu, qa, qx, qa2, qx2
 
 
-def measure_moe_down_rows(F, S, dev, flush, st, reps, warm, hbm_row, tensor_row, out, pk):
+def measure_moe_down_rows(F, S, dev, flush, st, reps, warm, hbm_row, grouped_row, out):
     E, k, P = 256, 8, F.FP8_SCALE_POW2
     md = S.moe_down(with_weights=False)
     h, logits = md["h"].to(dev), md["logits"].to(dev)
@@ -516,16 +524,12 @@ def measure_moe_down_rows(F, S, dev, flush, st, reps, warm, hbm_row, tensor_row,
     ms = _time(lambda: F.fp8_grouped_gemm_blockscaled(qh, sh, qwd, swd, r["off"], d=yd), reps, warm, flush, st)
     wbytes = E * Nd * Kd
     moved = wbytes + R * Kd + R * Nd * 2
-    tensor_row("a6_grouped_moe_down", ms, 2.0 * R * Nd * Kd, "32768 rows, 256 experts, N=7168, K=2048",
-               dict(weight_bytes=wbytes, hbm_achieved_gbs=round(moved / (ms * 1e-3) / 1e9, 1),
-                    hbm_frac=round(moved / (ms * 1e-3) / 1e9 / pk["hbm"], 4)))
+    grouped_row("a6_grouped_moe_down", ms, 2.0 * R * Nd * Kd, moved, wbytes, "32768 rows, 256 experts, N=7168, K=2048")
     qh2, sh2 = F.fp8_quant_act_1x128(h, flags=P)
     yd2 = torch.empty((R, Nd), dtype=torch.bfloat16, device=dev)
     ms = _time(lambda: F.fp8_grouped_gemm_blockscaled_pow2(qh2, sh2, qwd2, swd2, r["off"], d=yd2), reps, warm, flush, st)
-    tensor_row("f1_grouped_moe_down_pow2", ms, 2.0 * R * Nd * Kd,
-               "32768 rows, 256 experts, N=7168, K=2048, pow-2 scales (microscaled MMA)",
-               dict(weight_bytes=wbytes, hbm_achieved_gbs=round(moved / (ms * 1e-3) / 1e9, 1),
-                    hbm_frac=round(moved / (ms * 1e-3) / 1e9 / pk["hbm"], 4)))
+    grouped_row("f1_grouped_moe_down_pow2", ms, 2.0 * R * Nd * Kd, moved, wbytes,
+                "32768 rows, 256 experts, N=7168, K=2048, pow-2 scales (microscaled MMA)")
     del qwd2, qh2, yd2
     outc = torch.empty((Tn, Nd), dtype=torch.bfloat16, device=dev)
     ms = _time(lambda: F.fp8_moe_combine_bf16(yd, r["pos"], r["gate"], out=outc), reps, warm, flush, st)

@@ -783,8 +783,16 @@ extern "C" int fp8_gemm_blockscaled(const uint8_t* a, const float* sa, const uin
     return gemm_blockscaled_impl(a, sa, b, sb, b_scale_mode, d, d_dtype, M, N, K, nullptr, 0, stream);
 }
 
-extern "C" int fp8_gemm_split_plan(int64_t M, int64_t N, int64_t K, int pairs, int64_t workspace_bytes,
+// Columns of one 256-row pair tile of a GEMM form: every form uses 256 x 256
+// tiles (the grouped form runs them as 128 x 256 single-CTA tiles).
+extern "C" int fp8_gemm_tile_cols(int form) {
+    return form == FP8_GEMM_FORM_DENSE || form == FP8_GEMM_FORM_Q8 || form == FP8_GEMM_FORM_GROUPED ? kBN
+                                                                                                  : FP8_ERR_ARG;
+}
+
+extern "C" int fp8_gemm_split_plan(int form, int64_t M, int64_t N, int64_t K, int pairs, int64_t workspace_bytes,
                                    int64_t* split, int64_t* tail0, int64_t* launched_pairs) {
+    if (form != FP8_GEMM_FORM_DENSE && form != FP8_GEMM_FORM_Q8) return FP8_ERR_ARG;
     if (M <= 0 || N <= 0 || K <= 0 || pairs <= 0 || workspace_bytes < 0 || !split || !tail0 || !launched_pairs)
         return FP8_ERR_ARG;
     if (K % 128 || N % 128) return FP8_ERR_SHAPE;
@@ -796,10 +804,10 @@ extern "C" int fp8_gemm_split_plan(int64_t M, int64_t N, int64_t K, int pairs, i
     return FP8_OK;
 }
 
-extern "C" int64_t fp8_gemm_split_units(int64_t M, int64_t N, int64_t K, int pairs, int64_t workspace_bytes,
-                                        int64_t pair, int64_t* units, int64_t max_units) {
+extern "C" int64_t fp8_gemm_split_units(int form, int64_t M, int64_t N, int64_t K, int pairs,
+                                        int64_t workspace_bytes, int64_t pair, int64_t* units, int64_t max_units) {
     int64_t split, tail0, np;
-    const int rc = fp8_gemm_split_plan(M, N, K, pairs, workspace_bytes, &split, &tail0, &np);
+    const int rc = fp8_gemm_split_plan(form, M, N, K, pairs, workspace_bytes, &split, &tail0, &np);
     if (rc != FP8_OK) return rc;
     if (pair < 0 || pair >= np || max_units < 0 || (max_units > 0 && !units)) return FP8_ERR_ARG;
     const int64_t num_tiles = ((M + 2 * BM - 1) / (2 * BM)) * ((N + kBN - 1) / kBN);

@@ -31,6 +31,9 @@ FP8_BSCALE_BLOCK128 = 0
 FP8_BSCALE_ROW = 1
 FP8_OUT_BF16 = 0
 FP8_OUT_F32 = 1
+FP8_GEMM_FORM_DENSE = 0
+FP8_GEMM_FORM_Q8 = 1
+FP8_GEMM_FORM_GROUPED = 2
 FP8_ERR_TIMEOUT = -5
 FP8_ERR_OFFSETS = -6
 FP8_ERR_SCRATCH = -8
@@ -70,10 +73,12 @@ lib.fp8_moe_route_workspace_size.argtypes = [_I64, _I]
 lib.fp8_moe_route_workspace_size.restype = _I64
 lib.fp8_gemm_blockscaled_workspace_bytes.argtypes = [_I64, _I64, _I64]
 lib.fp8_gemm_blockscaled_workspace_bytes.restype = _I64
-lib.fp8_gemm_split_plan.argtypes = [_I64, _I64, _I64, _I, _I64, _P, _P, _P]
+lib.fp8_gemm_split_plan.argtypes = [_I, _I64, _I64, _I64, _I, _I64, _P, _P, _P]
 lib.fp8_gemm_split_plan.restype = _I
-lib.fp8_gemm_split_units.argtypes = [_I64, _I64, _I64, _I, _I64, _I64, _P, _I64]
+lib.fp8_gemm_split_units.argtypes = [_I, _I64, _I64, _I64, _I, _I64, _I64, _P, _I64]
 lib.fp8_gemm_split_units.restype = _I64
+lib.fp8_gemm_tile_cols.argtypes = [_I]
+lib.fp8_gemm_tile_cols.restype = _I
 lib.fp8_strerror.argtypes = [_I]
 lib.fp8_strerror.restype = ctypes.c_char_p
 lib.fp8_version.argtypes = []
@@ -81,7 +86,8 @@ lib.fp8_version.restype = _I
 
 #: every symbol include/fp8bs.h declares
 EXPORTED = sorted(list(_SIGS) + ["fp8_moe_route_workspace_size", "fp8_gemm_blockscaled_workspace_bytes",
-                                  "fp8_gemm_split_plan", "fp8_gemm_split_units", "fp8_strerror", "fp8_version"])
+                                  "fp8_gemm_split_plan", "fp8_gemm_split_units", "fp8_gemm_tile_cols",
+                                  "fp8_strerror", "fp8_version"])
 
 
 class FP8Error(RuntimeError):
@@ -212,21 +218,30 @@ def release_gemm_workspaces(_synchronize=torch.cuda.synchronize) -> int:
     return n
 
 
-def fp8_gemm_split_plan(M: int, N: int, K: int, pairs: int, workspace_bytes: int):
-    """(split, tail0, launched_pairs) of the dense GEMM's tail split (host only)."""
+def fp8_gemm_tile_cols(form: int = FP8_GEMM_FORM_DENSE) -> int:
+    """Columns of one 256-row output tile of a GEMM form (host only)."""
+    n = lib.fp8_gemm_tile_cols(form)
+    if n < 0:
+        _check("fp8_gemm_tile_cols", n)
+    return n
+
+
+def fp8_gemm_split_plan(M: int, N: int, K: int, pairs: int, workspace_bytes: int, form: int = FP8_GEMM_FORM_DENSE):
+    """(split, tail0, launched_pairs) of a dense GEMM form's tail split (host only)."""
     out = (ctypes.c_int64 * 3)()
     p = ctypes.addressof(out)
-    _check("fp8_gemm_split_plan", lib.fp8_gemm_split_plan(M, N, K, pairs, workspace_bytes, p, p + 8, p + 16))
+    _check("fp8_gemm_split_plan", lib.fp8_gemm_split_plan(form, M, N, K, pairs, workspace_bytes, p, p + 8, p + 16))
     return int(out[0]), int(out[1]), int(out[2])
 
 
-def fp8_gemm_split_units(M: int, N: int, K: int, pairs: int, workspace_bytes: int, pair: int):
+def fp8_gemm_split_units(M: int, N: int, K: int, pairs: int, workspace_bytes: int, pair: int,
+                         form: int = FP8_GEMM_FORM_DENSE):
     """[(tile, kb0, kb1, slab), ...] that launched pair `pair` runs (host only)."""
-    n = lib.fp8_gemm_split_units(M, N, K, pairs, workspace_bytes, pair, None, 0)
+    n = lib.fp8_gemm_split_units(form, M, N, K, pairs, workspace_bytes, pair, None, 0)
     if n < 0:
         _check("fp8_gemm_split_units", int(n))
     buf = (ctypes.c_int64 * (4 * max(n, 1)))()
-    lib.fp8_gemm_split_units(M, N, K, pairs, workspace_bytes, pair, ctypes.addressof(buf), n)
+    lib.fp8_gemm_split_units(form, M, N, K, pairs, workspace_bytes, pair, ctypes.addressof(buf), n)
     return [tuple(int(v) for v in buf[4 * i:4 * i + 4]) for i in range(n)]
 
 

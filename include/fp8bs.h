@@ -194,22 +194,33 @@ FP8_API int fp8_gemm_blockscaled(const uint8_t* a, const float* sa,
  * ---------------------------------------------------------------------- */
 FP8_API int64_t fp8_gemm_blockscaled_workspace_bytes(int64_t M, int64_t N, int64_t K);
 
-/* The tail-split plan of the dense GEMM above for `pairs` SM pairs and a
- * workspace of workspace_bytes (0: none): *split K ranges per split tile
- * (0: no split), *tail0 the first split tile (256 x 256 tiles numbered with
- * the 256-row tile index fastest), *launched_pairs the pairs the launch
- * uses.  Host-only arithmetic, no device access; the launch takes `pairs`
- * from the device's occupancy (148 SMs: 74).  FP8_ERR_ARG / _SHAPE as
- * fp8_gemm_blockscaled. */
-FP8_API int fp8_gemm_split_plan(int64_t M, int64_t N, int64_t K, int pairs, int64_t workspace_bytes,
+/* GEMM forms, for the tile and split-plan queries below. */
+#define FP8_GEMM_FORM_DENSE   0   /* fp8_gemm_blockscaled(_ws): bf16 or fp32 D */
+#define FP8_GEMM_FORM_Q8      1   /* fp8_gemm_blockscaled_q8(_ws): E4M3 D */
+#define FP8_GEMM_FORM_GROUPED 2   /* fp8_grouped_gemm_blockscaled */
+
+/* Columns of one output tile of a GEMM form (256 for every form: 256-row
+ * tiles on an SM pair for the dense forms, 128-row tiles on one SM for the
+ * grouped form).  FP8_ERR_ARG for an unknown form.  Host only. */
+FP8_API int fp8_gemm_tile_cols(int form);
+
+/* The tail-split plan of a dense GEMM form (FP8_GEMM_FORM_DENSE or _Q8) for
+ * `pairs` SM pairs and a workspace of workspace_bytes (0: none): *split K
+ * ranges per split tile (0: no split), *tail0 the first split tile (256-row
+ * tiles of fp8_gemm_tile_cols(form) columns, numbered with the 256-row tile
+ * index fastest), *launched_pairs the pairs the launch uses.  Host-only
+ * arithmetic, no device access; the launch takes `pairs` from the device's
+ * occupancy (148 SMs: 74).  FP8_ERR_ARG for another form, otherwise
+ * FP8_ERR_ARG / _SHAPE as fp8_gemm_blockscaled. */
+FP8_API int fp8_gemm_split_plan(int form, int64_t M, int64_t N, int64_t K, int pairs, int64_t workspace_bytes,
                                 int64_t* split, int64_t* tail0, int64_t* launched_pairs);
 
 /* The work units of launched pair `pair` under that plan, in the order the
  * pair runs them: units[4i .. 4i+3] = tile, first K block, end K block,
  * workspace slab (-1: whole tile, stored to D).  Writes at most max_units
  * units and returns how many the pair has (negative: an FP8_ERR_* code). */
-FP8_API int64_t fp8_gemm_split_units(int64_t M, int64_t N, int64_t K, int pairs, int64_t workspace_bytes,
-                                     int64_t pair, int64_t* units, int64_t max_units);
+FP8_API int64_t fp8_gemm_split_units(int form, int64_t M, int64_t N, int64_t K, int pairs,
+                                     int64_t workspace_bytes, int64_t pair, int64_t* units, int64_t max_units);
 FP8_API int fp8_gemm_blockscaled_ws(const uint8_t* a, const float* sa,
                                     const uint8_t* b, const float* sb, int b_scale_mode,
                                     void* d, int d_dtype, int64_t M, int64_t N, int64_t K,

@@ -1,13 +1,14 @@
 """GPU parity of the block-scaled GEMM when its last tiles are split along K
-(pages 2 and 3: the output is the sum over 128-element K blocks of the
+(the promotion passages of the tmdrlife.com and gnrental.net pages: the output is the sum over 128-element K blocks of the
 promoted, scaled tensor-core partial sums; a split only regroups that fp32
 sum into per-range sums that a second kernel adds in K order).
 
 Checks: every column of every 7th row of a split problem against the
-oracle's fp64 product; split against unsplit on the full dense-linear shape
-(identical bits on the tiles computed whole, fp32 regrouping error on the
-split ones); small problems split over the whole GPU, with ragged rows,
-half-used column tiles, canaries past D and two runs bit-identical.
+oracle's fp64 product; split against unsplit on a K = 7168 problem and on
+the Wgrad shape (identical bits on the tiles computed whole, fp32
+regrouping error on the split ones); small problems split over the whole
+GPU, with ragged rows, half-used column tiles, canaries past D and two runs
+bit-identical.
 """
 import numpy as np
 import pytest
@@ -51,11 +52,28 @@ def test_workspace_size_reports_one_slab_per_sm_pair(fb):
     assert fb.lib.fp8_gemm_blockscaled_workspace_bytes(4096, 7168, 1024) == 0     # too short to split
 
 
+def _split_mask(fb, M, N, K, form=0):
+    """Where D comes from split tiles under the library's plan on this GPU."""
+    pairs = torch.cuda.get_device_properties(0).multi_processor_count // 2
+    ws = fb.lib.fp8_gemm_blockscaled_workspace_bytes(M, N, K)
+    split, tail0, _ = fb.fp8_gemm_split_plan(M, N, K, pairs, ws, form)
+    bn = fb.fp8_gemm_tile_cols(form)
+    num_m2 = (M + 255) // 256
+    mask = np.zeros((M, N), dtype=bool)
+    for w in range(tail0, num_m2 * ((N + bn - 1) // bn)) if split else ():
+        r0, c0 = (w % num_m2) * 256, (w // num_m2) * bn
+        mask[r0:r0 + 256, c0:c0 + bn] = True
+    return split, mask
+
+
 @pytest.mark.parametrize("out_dtype", [torch.bfloat16, torch.float32])
 def test_split_tail_full_rows(fb, orc, out_dtype):
-    """4096 x 7168 x 2048: 448 tiles leave a last wave of 4 on 74 SM pairs,
-    which is split 8 ways; every column of every 7th row is checked."""
-    M, N, K = 4096, 7168, 2048
+    """4096 x 3840 x 2048: 16 x 15 tiles of 256 columns leave a short last
+    wave on 74 SM pairs, which is split along K; every column of every 7th
+    row is checked."""
+    M, N, K = 4096, 3840, 2048
+    split, mask = _split_mask(fb, M, N, K)
+    assert split > 0 and mask.any()
     a, sa, b, sb = _operands(M, N, K, 0, 21)
     rows = np.arange(0, M, 7)
     ref = orc.gemm_blockscaled(a, sa, b, sb, 0, rows=rows, cols=np.arange(N))
@@ -67,20 +85,19 @@ def test_split_tail_full_rows(fb, orc, out_dtype):
     assert _elementwise_ok(got, ref, bf16) == 0
 
 
-def test_split_matches_unsplit_dense_linear_shape(fb):
-    """The dense-linear shape (K = 7168, split 18 ways): the tiles computed
-    whole are bit-identical with and without the workspace; the split tiles
-    (last column tile, rows 3072..4095) agree within fp32 regrouping."""
-    if torch.cuda.get_device_properties(0).multi_processor_count // 2 != 74:
-        pytest.skip("the split tiles below assume 74 SM pairs")
-    M, N, K = 4096, 7168, 7168
-    a, sa, b, sb = _operands(M, N, K, 0, 33)
+@pytest.mark.parametrize("M,N,K,mode", [(4096, 3840, 7168, 0), (4096, 3840, 8192, 1)])
+def test_split_matches_unsplit(fb, M, N, K, mode):
+    """K = 7168 (block B scales) and K = 8192 (per-row B scales, the Wgrad
+    form) problems whose last wave is split: the tiles computed whole are
+    bit-identical with and without the workspace; the split tiles agree
+    within fp32 regrouping."""
+    split, tail = _split_mask(fb, M, N, K)
+    assert split > 0 and tail.any()
+    a, sa, b, sb = _operands(M, N, K, mode, 33)
     A, SA, B, SB = _dev(a), _dev(sa), _dev(b), _dev(sb)
-    d_split = fb.fp8_gemm_blockscaled(A, SA, B, SB, 0, torch.float32).cpu().numpy()
-    d_whole = fb.fp8_gemm_blockscaled(A, SA, B, SB, 0, torch.float32, split=False).cpu().numpy()
+    d_split = fb.fp8_gemm_blockscaled(A, SA, B, SB, mode, torch.float32).cpu().numpy()
+    d_whole = fb.fp8_gemm_blockscaled(A, SA, B, SB, mode, torch.float32, split=False).cpu().numpy()
     assert fb.fp8_get_status() == 0
-    tail = np.zeros((M, N), dtype=bool)
-    tail[3072:, 6912:] = True                     # tiles 444..447: rows 12..15 of column tile 27
     assert np.array_equal(d_split[~tail].view(np.uint32), d_whole[~tail].view(np.uint32))
     diff = np.abs(d_split[tail] - d_whole[tail])
     assert diff.max() <= 1e-5 * np.abs(d_whole).max(), diff.max()

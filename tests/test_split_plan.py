@@ -21,17 +21,23 @@ def fb():
     return fp8bs
 
 
-SLAB = 256 * 256 * 4
+SLAB = 256 * 256 * 4          # one pair tile of fp32 partial sums: what the workspace size counts per pair
+FORMS = [0, 1]                # FP8_GEMM_FORM_DENSE, FP8_GEMM_FORM_Q8
 
 
-def _walk(fb, M, N, K, pairs, ws_bytes):
-    split, tail0, np_ = fb.fp8_gemm_split_plan(M, N, K, pairs, ws_bytes)
-    num_tiles = ((M + 255) // 256) * ((N + 255) // 256)
+def _slab(fb, form):
+    return 256 * fb.fp8_gemm_tile_cols(form) * 4
+
+
+def _walk(fb, M, N, K, pairs, ws_bytes, form=0):
+    split, tail0, np_ = fb.fp8_gemm_split_plan(M, N, K, pairs, ws_bytes, form)
+    bn = fb.fp8_gemm_tile_cols(form)
+    num_tiles = ((M + 255) // 256) * ((N + bn - 1) // bn)
     nkb = K // 128
     seen = {}
     slabs = {}
     for c in range(np_):
-        units = fb.fp8_gemm_split_units(M, N, K, pairs, ws_bytes, c)
+        units = fb.fp8_gemm_split_units(M, N, K, pairs, ws_bytes, c, form)
         assert units, "pair %d has no work" % c
         for i, (w, kb0, kb1, slab) in enumerate(units):
             assert 0 <= w < num_tiles and 0 <= kb0 < kb1 <= nkb
@@ -53,9 +59,10 @@ def _walk(fb, M, N, K, pairs, ws_bytes):
                                    (640, 1280, 4096), (4096, 7168, 1024), (128, 256, 128), (10240, 256, 4096),
                                    (4096, 2048, 7168), (5000, 5120, 3072)])
 @pytest.mark.parametrize("pairs", [74, 72, 70, 66, 8, 1])
-def test_every_k_block_once_and_every_pair_busy(fb, M, N, K, pairs):
+@pytest.mark.parametrize("form", FORMS)
+def test_every_k_block_once_and_every_pair_busy(fb, M, N, K, pairs, form):
     ws = pairs * SLAB
-    split, tail0, np_, slabs, num_tiles, nkb = _walk(fb, M, N, K, pairs, ws)
+    split, tail0, np_, slabs, num_tiles, nkb = _walk(fb, M, N, K, pairs, ws, form)
     assert np_ <= pairs
     tail = num_tiles % pairs
     if split:
@@ -75,16 +82,23 @@ def test_every_k_block_once_and_every_pair_busy(fb, M, N, K, pairs):
             pytest.fail("a splittable last wave was not split")
 
 
+def test_tile_widths(fb):
+    # every form runs 256-column tiles (two 256-column TMEM accumulators)
+    assert [fb.fp8_gemm_tile_cols(f) for f in (0, 1, 2)] == [256, 256, 256]
+    assert fb.lib.fp8_gemm_tile_cols(3) == -1
+
+
 def test_known_plans(fb):
-    # the dense-linear GEMM on 74 pairs: 448 tiles, last wave of 4 cut into 18 ranges
-    assert fb.fp8_gemm_split_plan(4096, 7168, 7168, 74, 74 * SLAB) == (18, 444, 74)
-    # Wgrad: 784 tiles leave 44 on 74 pairs, more than half: whole tiles only
-    assert fb.fp8_gemm_split_plan(7168, 7168, 8192, 74, 74 * SLAB) == (0, 784, 74)
-    # one tile, 16 K blocks: 8 ranges of 2, 8 pairs launched
-    assert fb.fp8_gemm_split_plan(256, 256, 2048, 74, 74 * SLAB) == (8, 0, 8)
-    # no workspace, or too short a K: no split, one pair per tile at most
-    assert fb.fp8_gemm_split_plan(4096, 7168, 7168, 74, 0) == (0, 448, 74)
-    assert fb.fp8_gemm_split_plan(256, 256, 1024, 74, 74 * SLAB) == (0, 1, 1)
+    for form in FORMS:
+        # the dense-linear GEMM on 74 pairs: 448 tiles, last wave of 4 cut into 18 ranges
+        assert fb.fp8_gemm_split_plan(4096, 7168, 7168, 74, 74 * SLAB, form) == (18, 444, 74)
+        # Wgrad: 784 tiles leave 44 on 74 pairs, more than half: whole tiles only
+        assert fb.fp8_gemm_split_plan(7168, 7168, 8192, 74, 74 * SLAB, form) == (0, 784, 74)
+        # one tile, 16 K blocks: 8 ranges of 2, 8 pairs launched
+        assert fb.fp8_gemm_split_plan(256, 256, 2048, 74, 74 * SLAB, form) == (8, 0, 8)
+        # no workspace, or too short a K: no split, one pair per tile at most
+        assert fb.fp8_gemm_split_plan(4096, 7168, 7168, 74, 0, form) == (0, 448, 74)
+        assert fb.fp8_gemm_split_plan(256, 256, 1024, 74, 74 * SLAB, form) == (0, 1, 1)
 
 
 def test_small_workspace_disables_the_split(fb):
@@ -95,10 +109,12 @@ def test_small_workspace_disables_the_split(fb):
 
 def test_plan_argument_errors(fb):
     L = fb.lib
-    assert L.fp8_gemm_split_plan(0, 256, 256, 74, 0, None, None, None) == -1
+    assert L.fp8_gemm_split_plan(0, 0, 256, 256, 74, 0, None, None, None) == -1
     import ctypes
     out = (ctypes.c_int64 * 3)()
     p = ctypes.addressof(out)
-    assert L.fp8_gemm_split_plan(256, 200, 256, 74, 0, p, p + 8, p + 16) == -2
-    assert L.fp8_gemm_split_plan(256, 256, 256, 0, 0, p, p + 8, p + 16) == -1
-    assert L.fp8_gemm_split_units(256, 256, 2048, 74, 74 * SLAB, 8, None, 0) == -1   # pair beyond the launch
+    assert L.fp8_gemm_split_plan(0, 256, 200, 256, 74, 0, p, p + 8, p + 16) == -2
+    assert L.fp8_gemm_split_plan(0, 256, 256, 256, 0, 0, p, p + 8, p + 16) == -1
+    assert L.fp8_gemm_split_plan(2, 256, 256, 2048, 74, 0, p, p + 8, p + 16) == -1    # grouped: no split
+    assert L.fp8_gemm_split_plan(7, 256, 256, 2048, 74, 0, p, p + 8, p + 16) == -1    # unknown form
+    assert L.fp8_gemm_split_units(0, 256, 256, 2048, 74, 74 * SLAB, 8, None, 0) == -1    # pair beyond the launch
