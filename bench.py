@@ -1,6 +1,7 @@
 """Benchmark of the fine-grained FP8 path on B300.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference] [--rows all|none]
+    python bench.py --case NAME [--reps R]     (one kernel on a bounded case, for ncu captures)
 
 One step = one pass of the dense-linear workload through the whole path:
 1x128 quantisation of X [4096, 7168], 128x128 quantisation of W [7168, 7168]
@@ -329,7 +330,7 @@ def run_ours(args, ws, rank, local):
         out["rows"] = rows
         out["rows_clocks"] = rows_clocks
     if rank == 0 and ws == 1 and not args.no_cpu_baseline:
-        out["cpu_baseline"] = cpu_baseline(S, d=d)
+        out["cpu_baseline"] = cpu_baseline(S, d=d, dev=dev)
     return out
 
 
@@ -342,11 +343,44 @@ def gemm_launches(F, m, n, k, dev) -> int:
     return 2 if split > 0 else 1
 
 
+class _SmClock:
+    """The SM clock read through NVML right after each timed repetition, so
+    that every row carries the clock it ran at (a row measured at a lower
+    clock -- the power cap acting after the heavy rows -- shows as such)."""
+
+    def __init__(self):
+        self.h = None
+        self.last = None
+        try:
+            import pynvml
+            pynvml.nvmlInit()
+            self.nv = pynvml
+            self.h = pynvml.nvmlDeviceGetHandleByIndex(torch.cuda.current_device())
+        except Exception:
+            self.h = None
+
+    def read(self):
+        if self.h is None:
+            return None
+        try:
+            return float(self.nv.nvmlDeviceGetClockInfo(self.h, self.nv.NVML_CLOCK_SM))
+        except Exception:
+            return None
+
+
+_SM_CLOCK = None
+
+
 def _time(fn, reps, warm, flush, stream):
+    """Median of `reps` event-timed runs, L2 flushed before each; records the
+    median SM clock sampled after each run in _SM_CLOCK.last."""
+    global _SM_CLOCK
+    if _SM_CLOCK is None:
+        _SM_CLOCK = _SmClock()
     a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     for _ in range(warm):
         fn()
-    ts = []
+    ts, mhz = [], []
     for _ in range(reps):
         flush()
         a.record(stream)
@@ -354,7 +388,15 @@ def _time(fn, reps, warm, flush, stream):
         b.record(stream)
         b.synchronize()
         ts.append(a.elapsed_time(b))
+        c = _SM_CLOCK.read()
+        if c is not None:
+            mhz.append(c)
+    _SM_CLOCK.last = statistics.median(mhz) if mhz else None
     return statistics.median(ts)
+
+
+def _row_clock():
+    return None if _SM_CLOCK is None else _SM_CLOCK.last
 
 
 ROW_SECTIONS = ("dense", "wgrad", "moe_up", "moe_down", "swiglu")
@@ -372,7 +414,7 @@ def measure_rows(F, S, dev, flush, pk, sections=ROW_SECTIONS):
         gbs = nbytes / (ms * 1e-3) / 1e9
         out[name] = dict(workload=workload, ms=round(ms, 5), bound="hbm", achieved=round(gbs, 1), unit="GB/s",
                          algorithmic_bytes=int(nbytes), peak=pk["hbm"], frac=round(gbs / pk["hbm"], 4),
-                         frac_of_nominal_8000=round(gbs / HBM_NOMINAL_GBS, 4))
+                         frac_of_nominal_8000=round(gbs / HBM_NOMINAL_GBS, 4), sm_mhz=_row_clock())
 
     def grouped_row(name, ms, flop, moved, wbytes, workload):
         """A grouped GEMM streams every expert's weights once: HBM-bound (AI ~
@@ -384,13 +426,13 @@ def measure_rows(F, S, dev, flush, pk, sections=ROW_SECTIONS):
                          algorithmic_bytes=int(moved), weight_bytes=int(wbytes), peak=pk["hbm"],
                          frac=round(gbs / pk["hbm"], 4), frac_of_nominal_8000=round(gbs / HBM_NOMINAL_GBS, 4),
                          tflops=round(tf, 1), tensor_frac=round(tf / fp8_peak, 4),
-                         tensor_frac_of_nominal_4500=round(tf / FP8_NOMINAL_TFLOPS, 4))
+                         tensor_frac_of_nominal_4500=round(tf / FP8_NOMINAL_TFLOPS, 4), sm_mhz=_row_clock())
 
     def tensor_row(name, ms, flop, workload, extra=None):
         tf = flop / (ms * 1e-3) / 1e12
         r = dict(workload=workload, ms=round(ms, 5), bound="tensor", achieved=round(tf, 1), unit="TFLOP/s",
                  flop=flop, peak=round(fp8_peak, 1), frac=round(tf / fp8_peak, 4),
-                 frac_of_nominal_4500=round(tf / FP8_NOMINAL_TFLOPS, 4))
+                 frac_of_nominal_4500=round(tf / FP8_NOMINAL_TFLOPS, 4), sm_mhz=_row_clock())
         if extra:
             r.update(extra)
         out[name] = r
@@ -549,44 +591,158 @@ def measure_swiglu_rows(F, dev, flush, st, reps, warm, hbm_row):
 
 
 # ---------------------------------------------------------------- oracle (CPU) arm
-def cpu_baseline(S, rows=1024, cols=N, d=None):
-    """The oracle, as it stands, on a bounded sample of the dense-linear step:
-    1x128 quantisation of the first `rows` rows of X, 128x128 quantisation of
-    the first `cols` rows of W (whole 128-row panels), and the rows x cols
-    corner of the GEMM in fp64.  Reported as GEMM TFLOP/s of the sample."""
-    import oracle
-    oracle.build()
-    d = d or S.dense_linear()
+def _dense_sample(S, oracle, d, rows):
+    """1x128 quantisation of the first `rows` rows of X, 128x128 quantisation
+    of all of W, and those rows of the GEMM in fp64: seconds, FLOP."""
     xb = S.bf16_bits(d["x"][:rows])
-    wb = S.bf16_bits(d["w"][:cols])
+    wb = S.bf16_bits(d["w"])
     t0 = time.perf_counter()
     qa, sa = oracle.quant_act_1x128(xb)
     qb, sb = oracle.quant_weight_128x128(wb)
     oracle.gemm_blockscaled(qa, sa, qb, sb, 0)
     dt = time.perf_counter() - t0
-    flop = 2.0 * rows * cols * K
-    return {"value": round(flop / dt / 1e12, 6), "unit": "TFLOP/s", "cores": oracle.max_threads(),
-            "kind": "oracle", "seconds": round(dt, 2),
-            "sample": "%d of 4096 rows x %d of 7168 columns of the dense-linear step: quantise those X rows "
-                      "(1x128) and W rows (128x128), then that corner of the GEMM in fp64" % (rows, cols)}
+    return dt, 2.0 * rows * wb.shape[0] * xb.shape[1]
+
+
+def _rate(nbytes_or_flop, sec, unit):
+    scale = 1e9 if unit in ("GB/s", "GFLOP/s") else 1e12
+    return round(nbytes_or_flop / sec / scale, 4)
+
+
+def cpu_baseline(S, d=None, dev=None):
+    """The oracle, as it stands, on the host's cores (OpenMP, all threads), on
+    a bounded sample of every workload (about 10-20 s of CPU work in all):
+    quantisers, routing, dispatch and combine on the full tensors, GEMMs in
+    fp64 on a stated fixed part of the rows.  `value` is the dense-linear
+    step's sample (512 of 4096 rows with all of W) as GEMM TFLOP/s; `configs`
+    has each workload's steps with their own rates."""
+    import numpy as np
+    import oracle
+    oracle.build()
+    cores = oracle.max_threads()
+    T = time.perf_counter
+
+    def step(fn, amount, unit, what):
+        t0 = T()
+        out = fn()
+        dt = T() - t0
+        return out, dict(seconds=round(dt, 3), value=_rate(amount, dt, unit), unit=unit, sample=what)
+
+    cfgs = {}
+    # tiny dense (everything in full)
+    td = S.tiny_dense()
+    xb, wb = S.bf16_bits(td["x"]), S.bf16_bits(td["w"])
+    c = {}
+    (qa, sa), c["quant_act_1x128"] = step(lambda: oracle.quant_act_1x128(xb), xb.size * 3, "GB/s", "X [128,512], all")
+    (qb, sb), c["quant_weight_128x128"] = step(lambda: oracle.quant_weight_128x128(wb), wb.size * 3, "GB/s",
+                                               "W [256,512], all")
+    _, c["gemm_fp64"] = step(lambda: oracle.gemm_blockscaled(qa, sa, qb, sb, 0), 2.0 * 128 * 256 * 512, "GFLOP/s",
+                             "128x256x512, all")
+    cfgs["tiny_dense"] = c
+    # dense linear: quantisers in full, GEMM on 512 of 4096 rows
+    d = d or S.dense_linear()
+    xb, wb = S.bf16_bits(d["x"]), S.bf16_bits(d["w"])
+    c = {}
+    (qa, sa), c["quant_act_1x128"] = step(lambda: oracle.quant_act_1x128(xb), xb.size * 3, "GB/s",
+                                          "X [4096,7168], all")
+    (qb, sb), c["quant_weight_128x128"] = step(lambda: oracle.quant_weight_128x128(wb), wb.size * 3, "GB/s",
+                                               "W [7168,7168], all")
+    rows = np.arange(512)
+    _, c["gemm_fp64"] = step(lambda: oracle.gemm_blockscaled(qa, sa, qb, sb, 0, rows=rows), 2.0 * 512 * N * K,
+                             "GFLOP/s", "rows 0..511 of 4096 x all 7168 columns, K 7168")
+    cfgs["dense_linear"] = c
+    head_dt, head_flop = _dense_sample(S, oracle, d, 512)
+    del d, xb, wb, qa, qb
+    # MoE up-projection: routing, quantisation and dispatch in full; 4 experts'
+    # weights quantised; the grouped GEMM on the rows of 2 experts x all 4096 columns
+    mu = S.moe_up(with_weights=False)
+    c = {}
+    r, c["route_topk"] = step(lambda: oracle.route_topk(mu["logits"].numpy(), 8), 4096 * 256 * 4, "GB/s",
+                              "logits [4096,256] -> top-8, all")
+    xb = S.bf16_bits(mu["x"])
+    (qx, sx), c["quant_act_1x128"] = step(lambda: oracle.quant_act_1x128(xb), xb.size * 3, "GB/s",
+                                          "X [4096,7168], all")
+    (qa, sa), c["permute_rows"] = step(lambda: oracle.permute_rows(qx, sx, r["src_row"]), 2 * 32768 * (7168 + 224),
+                                       "GB/s", "[4096,7168] -> [32768,7168], all")
+    wdev = dev if dev is not None else "cpu"
+    wq = {}
+    wsample = [S.bf16_bits(S.expert_weight(0, e, 4096, 7168, device=wdev)) for e in range(4)]
+    _, c["quant_weight_128x128"] = step(lambda: [wq.__setitem__(e, oracle.quant_weight_128x128(w))
+                                                 for e, w in enumerate(wsample)],
+                                        4 * 4096 * 7168 * 3, "GB/s", "experts 0..3 of 256, [4096,7168] each")
+    off = r["off"]
+    lo, hi = int(off[0]), int(off[2])
+    _, c["grouped_gemm_fp64"] = step(
+        lambda: [oracle.gemm_blockscaled(qa[off[e]:off[e + 1]], np.ascontiguousarray(sa[:, off[e]:off[e + 1]]),
+                                         wq[e][0], wq[e][1], 0) for e in range(2)],
+        2.0 * (hi - lo) * 4096 * 7168, "GFLOP/s", "experts 0, 1 (%d rows) x all 4096 columns, K 7168" % (hi - lo))
+    cfgs["moe_up"] = c
+    del mu, xb, qx, qa, wq, wsample
+    # MoE down-projection: routing, quantisation and combine in full; 4
+    # experts' weights; the grouped GEMM on the rows of 2 experts
+    md = S.moe_down(with_weights=False)
+    c = {}
+    r, c["route_topk"] = step(lambda: oracle.route_topk(md["logits"].numpy(), 8), 4096 * 256 * 4, "GB/s",
+                              "logits [4096,256] -> top-8, all")
+    hb = S.bf16_bits(md["h"])
+    (qh, sh), c["quant_act_1x128"] = step(lambda: oracle.quant_act_1x128(hb), hb.size * 3, "GB/s",
+                                          "h [32768,2048], all")
+    wq = {}
+    wsample = [S.bf16_bits(S.expert_weight(1, e, 7168, 2048, device=wdev)) for e in range(4)]
+    _, c["quant_weight_128x128"] = step(lambda: [wq.__setitem__(e, oracle.quant_weight_128x128(w))
+                                                 for e, w in enumerate(wsample)],
+                                        4 * 7168 * 2048 * 3, "GB/s", "experts 0..3 of 256, [7168,2048] each")
+    off = r["off"]
+    lo, hi = int(off[0]), int(off[2])
+    _, c["grouped_gemm_fp64"] = step(
+        lambda: [oracle.gemm_blockscaled(qh[off[e]:off[e + 1]], np.ascontiguousarray(sh[:, off[e]:off[e + 1]]),
+                                         wq[e][0], wq[e][1], 0) for e in range(2)],
+        2.0 * (hi - lo) * 7168 * 2048, "GFLOP/s", "experts 0, 1 (%d rows) x all 7168 columns, K 2048" % (hi - lo))
+    yb = S.bf16_bits(torch.randn((32768, 7168), generator=torch.Generator().manual_seed(44)).to(torch.bfloat16))
+    _, c["combine_bf16"] = step(lambda: oracle.moe_combine(yb, r["pos"], r["gate"]),
+                                32768 * 7168 * 2 + 4096 * 7168 * 2, "GB/s",
+                                "expert outputs [32768,7168] -> [4096,7168], all")
+    cfgs["moe_down"] = c
+    del md, hb, qh, wq, wsample, yb
+    # Wgrad: both 128x1 quantisations in full; the GEMM on 64 of 7168 rows
+    wg = S.wgrad()
+    c = {}
+    dyb, xb = S.bf16_bits(wg["dy"]), S.bf16_bits(wg["x"])
+    (qa, sa), c["quant_act_128x1_dy"] = step(lambda: oracle.quant_act_128x1(dyb), dyb.size * 3, "GB/s",
+                                             "dY [8192,7168] -> dY^T, all")
+    (qb, sb), c["quant_act_128x1_x"] = step(lambda: oracle.quant_act_128x1(xb), xb.size * 3, "GB/s",
+                                            "X [8192,7168] -> X^T, all")
+    rows = np.arange(64)
+    _, c["gemm_fp64"] = step(lambda: oracle.gemm_blockscaled(qa, sa, qb, sb, 1, rows=rows),
+                             2.0 * 64 * 7168 * 8192, "GFLOP/s", "rows 0..63 of 7168 x all 7168 columns, K 8192")
+    cfgs["wgrad"] = c
+    total = sum(v["seconds"] for c in cfgs.values() for v in c.values()) + head_dt
+    return {"value": round(head_flop / head_dt / 1e12, 6), "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+            "seconds": round(head_dt, 2),
+            "sample": "dense-linear step on 512 of 4096 rows: quantise those X rows (1x128) and all of W "
+                      "(128x128), then those rows of the GEMM in fp64",
+            "seconds_all_configs": round(total, 1), "configs": cfgs}
 
 
 def run_reference(args, ws, rank):
     from fp8_fine_grained_16_b300 import synthetic as S
     if rank != 0:
         return None
-    per = []
-    cb = None
+    import oracle
+    oracle.build()
     d = S.dense_linear()
-    rows, cols = 32, 1024            # per step: about 0.1 s of oracle work on 8 cores
+    per = []
+    rows = 32                       # per step: about 0.1-0.5 s of oracle work
+    d_small = dict(x=d["x"][:rows], w=d["w"][:1024])
     for i in range(args.warmup + args.steps):
-        cb = cpu_baseline(S, rows=rows, cols=cols, d=d)
+        dt, flop = _dense_sample(S, oracle, d_small, rows)
         if i >= args.warmup:
-            per.append(cb["seconds"])
-    flop = 2.0 * rows * cols * K
+            per.append(dt)
     ms = 1e3 * sum(per) / len(per)
     v = round(flop / (ms * 1e-3) / 1e12, 6)
-    cb["value"] = v
+    cb = {"value": v, "unit": "TFLOP/s", "cores": oracle.max_threads(), "kind": "oracle",
+          "sample": "each step: 1x128 quantisation of 32 of 4096 X rows, 128x128 quantisation of 1024 of 7168 W "
+                    "rows, and that 32 x 1024 corner of the dense-linear GEMM in fp64"}
     return {
         "impl": "reference", "metric": METRIC, "value": v, "unit": "TFLOP/s", "n_gpus": ws,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 3), "higher_is_better": True,
@@ -598,6 +754,129 @@ def run_reference(args, ws, rank):
     }
 
 
+# ---------------------------------------------------------------- single-kernel cases (for ncu)
+CASES = ("dense", "wgrad", "wgrad_small", "q8", "dgrad_transpose", "quant_1x128", "quant_128x1", "quant_128x128",
+         "grouped_up_small", "grouped_down_small", "permute", "combine", "swiglu", "pow2_dense")
+
+
+def run_case(name: str, reps: int):
+    """One kernel of the path on a bounded synthetic case, launched 1 + reps
+    times (the first launch warms up): what an ncu capture of that kernel
+    runs (`-k <kernel> -s 1 -c 1`).  Random E4M3 codes (NaN codes excluded)
+    and log-uniform scales stand in for quantised operands; the grouped
+    cases keep the MoE shapes with 32 experts of ~128 rows (Poisson) so a
+    full-metric capture holds about 1 GB."""
+    from fp8_fine_grained_16_b300 import build
+    build.build()
+    from fp8_fine_grained_16_b300 import fp8bs as F
+    dev = torch.device("cuda", 0)
+    g = torch.Generator(device=dev).manual_seed(0)
+
+    def codes(*shape):
+        c = torch.randint(0, 256, shape, dtype=torch.uint8, device=dev, generator=g)
+        c[(c & 0x7F) == 0x7F] = 0x3C
+        return c
+
+    def scales(*shape):
+        return torch.exp(torch.empty(shape, device=dev).uniform_(-6.9, 1.38, generator=g))
+
+    def bf16(*shape):
+        return torch.randn(shape, device=dev, generator=g).to(torch.bfloat16)
+
+    def offsets(E, mean=128):
+        cnt = torch.poisson(torch.full((E,), float(mean), device=dev), generator=g).to(torch.int64)
+        off = torch.zeros(E + 1, dtype=torch.int32, device=dev)
+        off[1:] = torch.cumsum(cnt, 0).to(torch.int32)
+        return off, int(off[-1])
+
+    if name in ("dense", "q8", "pow2_dense"):
+        a, b = codes(M, K), codes(N, K)
+        sa, sb = scales(K // 128, M), scales(N // 128, K // 128)
+        if name == "pow2_dense":
+            sa, sb = torch.exp2(torch.round(torch.log2(sa))), torch.exp2(torch.round(torch.log2(sb)))
+            y = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+            fn = lambda: F.fp8_gemm_blockscaled_pow2(a, sa, b, sb, 0, torch.bfloat16, d=y)
+        elif name == "q8":
+            q8, s8 = F.fp8_gemm_blockscaled_q8(a, sa, b, sb)
+            fn = lambda: F.fp8_gemm_blockscaled_q8(a, sa, b, sb, 0, 0, q8, s8)
+        else:
+            y = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+            fn = lambda: F.fp8_gemm_blockscaled(a, sa, b, sb, 0, torch.bfloat16, d=y)
+        work = "%dx%dx%d" % (M, N, K)
+    elif name in ("wgrad", "wgrad_small"):
+        H, T = (7168, 8192) if name == "wgrad" else (2048, 8192)
+        a, b = codes(H, T), codes(H, T)
+        sa, sb = scales(T // 128, H), scales(T // 128, H)
+        dw = torch.empty((H, H), dtype=torch.float32, device=dev)
+        fn = lambda: F.fp8_gemm_blockscaled(a, sa, b, sb, F.FP8_BSCALE_ROW, torch.float32, d=dw)
+        work = "%dx%dx%d, per-row B scales, fp32 out" % (H, H, T)
+    elif name == "dgrad_transpose":
+        q, sq = codes(N, K), scales(N // 128, K // 128)
+        qT, sT = F.fp8_transpose_128x128(q, sq)
+        fn = lambda: F.fp8_transpose_128x128(q, sq, qT, sT)
+        work = "W codes [7168,7168] -> W^T codes"
+    elif name == "quant_1x128":
+        x = bf16(M, K)
+        qx, sx = F.fp8_quant_act_1x128(x)
+        fn = lambda: F.fp8_quant_act_1x128(x, qx, sx)
+        work = "X [4096,7168]"
+    elif name == "quant_128x1":
+        x = bf16(8192, 7168)
+        qT, sT = F.fp8_quant_act_128x1(x)
+        fn = lambda: F.fp8_quant_act_128x1(x, qT, sT)
+        work = "dY [8192,7168] -> dY^T"
+    elif name == "quant_128x128":
+        w = bf16(N, K)
+        qw, sw = F.fp8_quant_weight_128x128(w)
+        fn = lambda: F.fp8_quant_weight_128x128(w, qw, sw)
+        work = "W [7168,7168]"
+    elif name in ("grouped_up_small", "grouped_down_small"):
+        E = 32
+        Ng, Kg = (4096, 7168) if name == "grouped_up_small" else (7168, 2048)
+        off, R = offsets(E)
+        a, sa = codes(R, Kg), scales(Kg // 128, R)
+        b, sb = codes(E, Ng, Kg), scales(E, Ng // 128, Kg // 128)
+        y = torch.empty((R, Ng), dtype=torch.bfloat16, device=dev)
+        fn = lambda: F.fp8_grouped_gemm_blockscaled(a, sa, b, sb, off, d=y)
+        work = "%d rows, 32 experts, N=%d, K=%d" % (R, Ng, Kg)
+    elif name in ("permute", "combine"):
+        logits = torch.randn((4096, 256), device=dev, generator=g)
+        r = F.fp8_moe_route_topk(logits, 8)
+        if name == "permute":
+            q, sq = codes(4096, 7168), scales(56, 4096)
+            qo, so = F.fp8_permute_rows(q, sq, r["src_row"])
+            fn = lambda: F.fp8_permute_rows(q, sq, r["src_row"], qo, so)
+            work = "[4096,7168] fp8 -> [32768,7168] by top-8 of 256"
+        else:
+            y = bf16(32768, 7168)
+            out = F.fp8_moe_combine_bf16(y, r["pos"], r["gate"])
+            fn = lambda: F.fp8_moe_combine_bf16(y, r["pos"], r["gate"], out=out)
+            work = "[32768,7168] bf16 -> [4096,7168]"
+    elif name == "swiglu":
+        yup = bf16(32768, 4096)
+        qg, sg = F.fp8_swiglu_quant_1x128(yup, 2048)
+        fn = lambda: F.fp8_swiglu_quant_1x128(yup, 2048, qg, sg)
+        work = "[32768, 2 x 2048] bf16"
+    else:
+        raise SystemExit("unknown case %r (one of %s)" % (name, ", ".join(CASES)))
+    st = torch.cuda.current_stream()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    fn()
+    torch.cuda.synchronize()
+    ts = []
+    for _ in range(reps):
+        e0.record(st)
+        fn()
+        e1.record(st)
+        e1.synchronize()
+        ts.append(e0.elapsed_time(e1))
+    status = F.fp8_get_status()
+    print(json.dumps({"case": name, "workload": work, "launches": 1 + reps, "ms_min": round(min(ts), 5),
+                      "ms_median": round(statistics.median(ts), 5), "status": status}))
+    if status != 0:
+        raise SystemExit(1)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -607,7 +886,13 @@ def main():
     ap.add_argument("--rows", default="all",
                     help="all | none | comma-separated sections of %s" % ",".join(ROW_SECTIONS))
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--case", choices=CASES,
+                    help="run one kernel on a bounded synthetic case (1 + --reps launches) and exit")
+    ap.add_argument("--reps", type=int, default=3)
     args = ap.parse_args()
+    if args.case:
+        run_case(args.case, args.reps)
+        return
     if args.warmup < 3:
         args.warmup = 3
     ws, rank, local = dist_env()

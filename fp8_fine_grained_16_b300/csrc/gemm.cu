@@ -103,6 +103,17 @@ struct GemmArgs {
 // Output forms of the GEMM.
 constexpr int kOutBF16 = 0, kOutF32 = 1, kOutE4M3 = 2;
 
+// With per-column B scales (the Wgrad form, BMODE 1) every element of P_kb
+// takes its own product of a row and a column scale, and a thread that owns
+// one row x 128 columns must receive 128 column scales per K block from
+// shared memory (the warp's 32 threads all need the same ones).  That
+// broadcast, 128 KB per CTA per K block, is what bounds the promotion.  The
+// two-row promotion reads P_kb with the 16-lane TMEM load (tcgen05.ld.16x256b),
+// which gives each thread two rows x 64 columns: half the column scales per
+// thread for the same number of elements.  The E4M3 output keeps the
+// one-row layout, whose thread holds a whole 1x128 output tile.
+__host__ __device__ constexpr bool two_row_promotion(int bmode, int out) { return bmode == 1 && out != kOutE4M3; }
+
 struct Tile {
     int64_t row0;            // first row of the tile (global row index)
     int64_t row_end;         // rows >= row_end are not stored
@@ -144,7 +155,7 @@ constexpr int kSingleStages = 4;     // one CTA holds all 256 B rows: 48 KB of o
 constexpr int kPairRegsWG0 = 64, kPairRegsPromo = 216;
 static_assert(128 * kPairRegsWG0 + 256 * kPairRegsPromo <= kThreads * 168, "register split");
 
-template <bool PAIR, int BN, int STAGES, int BMODE, bool GROUPED>
+template <bool PAIR, int BN, int STAGES, int BMODE, bool GROUPED, bool TWO_ROW = false>
 struct PairLayout {
     static constexpr int kABytes = BM * BK;                      // this CTA's 128 rows
     static constexpr int kBBytes = (PAIR ? BN / 2 : BN) * BK;    // this CTA's half of B (all of it alone)
@@ -165,7 +176,8 @@ struct PairLayout {
     static constexpr int kPrivOff = (kMiscOff + 16 + 15) & ~15;
     static constexpr int kPrivRowBytes = kPromoWarps * 32 * 4;
     static constexpr int kPrivColOff = kPrivOff + kPrivRowBytes;
-    static constexpr int kPrivColBytes = BMODE == 1 ? 2 * kPromoWarps * (BN / 2) * 4 : 0;
+    // (with the two-row promotion every warp holds all BN column scales)
+    static constexpr int kPrivColBytes = BMODE == 1 ? 2 * kPromoWarps * (TWO_ROW ? BN : BN / 2) * 4 : 0;
     static constexpr int kGrpOff = kPrivColOff + kPrivColBytes;
     static constexpr int kGrpBytes = GROUPED ? 2 * (kMaxExperts + 1) * 4 : 0;
     static constexpr int kBytes = kGrpOff + kGrpBytes;
@@ -216,7 +228,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                      const __grid_constant__ CUtensorMap tmSA, const __grid_constant__ CUtensorMap tmSB,
                      const GemmArgs args) {
-    using L = PairLayout<PAIR, BN, STAGES, BMODE, GROUPED>;
+    // Per-column B scales (BMODE 1, bf16/fp32 out): the two-row promotion
+    constexpr bool kTwoRow = two_row_promotion(BMODE, OUT);
+    using L = PairLayout<PAIR, BN, STAGES, BMODE, GROUPED, kTwoRow>;
     static_assert(2 * BN <= kTmemCols, "two accumulators must fit in TMEM");
     static_assert(BN == 256, "one promotion half = 128 columns = one scale block and one column per warpgroup thread");
     constexpr int kHalf = BN / 2;
@@ -307,6 +321,130 @@ __global__ void __launch_bounds__(kThreads, 1)
     auto sb_row = [&](const Tile& t, int h) -> int64_t {
         const int64_t c0 = int64_t(t.n0) + h * kHalf;
         return (int64_t(t.e) * (args.N / 128) + (c0 < args.N ? c0 : args.N - 1) / 128) * nkb;
+    };
+
+    // The two-row promotion (per-column B scales, bf16/fp32 out).  Warp
+    // (w%4 = q, (w-4)/4 = hh) reads TMEM lanes 32q + 16hh .. +15 across all BN
+    // columns with the 16x256b shape: thread t owns rows ra = 32q + 16hh + t/4
+    // and ra + 8 of the CTA's 128 and, in every group of 8 columns, columns
+    // 2(t%4) and 2(t%4) + 1 (64 columns of the 256).  Per K block it copies the
+    // BN column scales into its own buffer (two 16-byte pieces per lane), frees
+    // the stage, loads P_kb in two 128-column halves (64 registers each),
+    // frees the accumulator after the second, and adds P * sB(column) * sA(row)
+    // into 2 x 64 fp32 registers with packed two-lane operations.
+    auto promote_two_rows = [&]() {
+        const int wq = warp & 3, hh = (warp - 4) >> 2;
+        const int lb = 32 * wq + 16 * hh;                  // first TMEM lane of this warp
+        const int ra = lb + (lane >> 2), rb = ra + 8;      // the thread's two rows (of the CTA's 128)
+        const int cp = 2 * (lane & 3);                      // its column pair in each group of 8
+        const uint32_t t_lane = uint32_t(lb) << 16;
+        const uint32_t full0 = PAIR ? mapa_shared(&full[0], 0) : smem_u32(&full[0]);
+        auto release = [&](uint32_t stage_i) {
+            if constexpr (PAIR) mbar_arrive_cluster(full0 + stage_i * 8); else mbar_arrive(&full[stage_i]);
+        };
+        __syncwarp();
+        if (lane == 0) {
+            release(0);
+            release(1);
+        }
+        uint32_t g = 0;
+        bool ok = true;
+        for (int64_t ui = 0; ok && ui < n_units; ++ui) {
+            const WorkUnit u = unit_at(ui);
+            const Tile t = tile_at(u.w);
+            const int sa_off0 = int(t.row0 & 3), m_step = int(args.M & 3);
+            float2 acc_a[BN / 8], acc_b[BN / 8];
+#pragma unroll
+            for (int i = 0; i < BN / 8; ++i) acc_a[i] = acc_b[i] = make_float2(0.0f, 0.0f);
+
+            for (int kb = int(u.kb0); kb < int(u.kb1); ++kb) {
+                const uint32_t stage = g % STAGES, phase = (g / STAGES) & 1u;
+                const uint32_t buf = g & 1u;
+                bool got = true;
+                if (lane == 0) got = mbar_wait_bounded(&sfull[stage], phase, abort_s);
+                got = __shfl_sync(0xFFFFFFFFu, got ? 1 : 0, 0) != 0;
+                __syncwarp();
+                if (!got) { ok = false; break; }
+                tc_fence_after();
+
+                const uint8_t* st = smem + stage * L::kStageBytes;
+                const float* sab = reinterpret_cast<const float*>(st + L::kSaOff) + ((sa_off0 + kb * m_step) & 3);
+                const float sa0 = sab[ra], sa1 = sab[rb];
+                // this K block's copy of the BN column scales (buffer g % 2, last
+                // read two K blocks ago); each value read from the stage goes into
+                // a store of this warp before the stage is freed
+                float* sbk = reinterpret_cast<float*>(smem + L::kPrivColOff) + ((g & 1u) * kPromoWarps + (warp - 4)) * BN;
+#pragma unroll
+                for (int i = 0; i < BN / 128; ++i)
+                    reinterpret_cast<float4*>(sbk)[lane + 32 * i] =
+                        reinterpret_cast<const float4*>(st + L::kSbOff)[lane + 32 * i];
+                float* row_slot = reinterpret_cast<float*>(smem + L::kPrivOff) + (warp - 4) * 32 + lane;
+                *row_slot = sa0 + sa1;
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&empty[stage]);
+
+                const float2 s0 = make_float2(sa0, sa0), s1 = make_float2(sa1, sa1);
+                auto scale_half = [&](int hc, const uint32_t (&v)[64]) {
+#pragma unroll
+                    for (int k = 0; k < 16; ++k) {
+                        const int grp = 16 * hc + k;
+                        const float2 sb = *reinterpret_cast<const float2*>(sbk + 8 * grp + cp);
+                        const float2 pa = __fmul2_rn(make_float2(__uint_as_float(v[4 * k]), __uint_as_float(v[4 * k + 1])), sb);
+                        const float2 pb =
+                            __fmul2_rn(make_float2(__uint_as_float(v[4 * k + 2]), __uint_as_float(v[4 * k + 3])), sb);
+                        acc_a[grp] = __ffma2_rn(pa, s0, acc_a[grp]);
+                        acc_b[grp] = __ffma2_rn(pb, s1, acc_b[grp]);
+                    }
+                };
+                const uint32_t tcol = tmem_base + t_lane + buf * BN;
+                uint32_t v[64];
+                tmem_ld_16x256b_x16(tcol, v);
+                tmem_wait_ld_regs64(v);
+                scale_half(0, v);
+                tmem_ld_16x256b_x16(tcol + 128, v);
+                tmem_wait_ld_regs64(v);
+                tc_fence_before();
+                __syncwarp();
+                // all of P_kb for this warp's 16 lanes is in registers:
+                // accumulator `buf` is free for K block g + 2
+                if (lane == 0) release((g + 2) % STAGES);
+                scale_half(1, v);
+                ++g;
+            }
+            if (!ok) break;
+
+            if constexpr (!GROUPED) {
+                if (u.slab >= 0) {
+                    // K range of a split tile: the whole 256 x BN partial goes
+                    // to its slab; the fix-up kernel adds the slabs
+                    float* dst_a = args.ws + (u.slab * kTileRows + int64_t(rank) * BM + ra) * BN + cp;
+                    float* dst_b = dst_a + 8 * BN;
+#pragma unroll
+                    for (int grp = 0; grp < BN / 8; ++grp) {
+                        *reinterpret_cast<float2*>(dst_a + 8 * grp) = acc_a[grp];
+                        *reinterpret_cast<float2*>(dst_b + 8 * grp) = acc_b[grp];
+                    }
+                    continue;
+                }
+            }
+#pragma unroll
+            for (int rr = 0; rr < 2; ++rr) {
+                const int64_t m = t.row0 + (rr ? rb : ra);
+                if (m >= t.row_end || m >= args.M) continue;
+                const float2* acc = rr ? acc_b : acc_a;
+#pragma unroll
+                for (int grp = 0; grp < BN / 8; ++grp) {
+                    const int64_t n = int64_t(t.n0) + 8 * grp + cp;
+                    if (n >= args.N) break;
+                    if constexpr (OUT == kOutF32)
+                        *reinterpret_cast<float2*>(reinterpret_cast<float*>(args.d) + m * args.N + n) = acc[grp];
+                    else
+                        *reinterpret_cast<uint32_t*>(reinterpret_cast<uint16_t*>(args.d) + m * args.N + n) =
+                            cvt_bf16x2(acc[grp].x, acc[grp].y);
+                }
+            }
+        }
+        if (!ok) record_status(FP8_ERR_TIMEOUT);
     };
 
     if (warp < 4) {
@@ -420,6 +558,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     } else {
         asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kPairRegsPromo));
         // ================= promotion warpgroups (each CTA, its own 128 rows)
+        if constexpr (kTwoRow) {
+            promote_two_rows();
+        } else {
         const int wq = warp & 3;
         const int half = (warp - 4) >> 2;
         const int r = wq * 32 + lane;
@@ -599,6 +740,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
         }
         if (!ok) record_status(FP8_ERR_TIMEOUT);
+        }
     }
 
     // ---------------- tear-down: neither CTA leaves (or frees TMEM) while the
@@ -670,7 +812,7 @@ static int64_t split_workspace_bytes(int sms, int64_t K) {
 template <bool PAIR, int BN, int STAGES, int BMODE, int OUT, bool GROUPED>
 static int launch_pair(const CUtensorMap& ma, const CUtensorMap& mb, const CUtensorMap& msa, const CUtensorMap& msb,
                        GemmArgs args, int sms, cudaStream_t stream, int64_t ws_bytes = 0) {
-    using L = PairLayout<PAIR, BN, STAGES, BMODE, GROUPED>;
+    using L = PairLayout<PAIR, BN, STAGES, BMODE, GROUPED, two_row_promotion(BMODE, OUT)>;
     auto kern = gemm_pair_kernel<PAIR, BN, STAGES, BMODE, OUT, GROUPED>;
     static unsigned char smem_opted_in[kMaxDevices] = {};
     if (!opt_in_dynamic_smem(kern, L::kDynSmem, smem_opted_in)) return FP8_ERR_CUDA;

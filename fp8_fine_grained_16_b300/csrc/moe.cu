@@ -6,7 +6,9 @@
 //             softmax gates over the selected logits, and a stable
 //             counting sort of (token, slot) pairs by expert:
 //               kernel 1: one warp per token -> idx, gate, per-chunk counts
-//               kernel 2: per chunk of 64 tokens -> expert offsets and the
+//               kernel 2: one thread per expert turns the counts into
+//                         running totals over the chunks, in place
+//               kernel 3: per chunk of 64 tokens -> expert offsets and the
 //                         rank of each pair among the chunk's pairs of the
 //                         same expert (64-bit token masks + popcount)
 //   permute   gathers FP8 rows and their K-block scales (dispatch)
@@ -93,9 +95,36 @@ __global__ void __launch_bounds__(256) route_topk_kernel(const float* __restrict
 }
 
 // ------------------------------------------------------------------ routing, kernel 2
+// work[c][e] (pairs of chunk c that chose expert e) -> the running total over
+// chunks 0..c, in place.  One thread per expert walks the chunks; the loads
+// of a warp are one 128-byte row segment, eight chunks in flight.
+__global__ void __launch_bounds__(256) route_chunk_scan_kernel(int32_t* __restrict__ work, int64_t nchunks, int E) {
+    const int e = blockIdx.x * blockDim.x + threadIdx.x;
+    if (e >= E) return;
+    int run = 0;
+    int64_t c = 0;
+    for (; c + 8 <= nchunks; c += 8) {
+        int v[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) v[i] = work[(c + i) * E + e];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            run += v[i];
+            work[(c + i) * E + e] = run;
+        }
+    }
+    for (; c < nchunks; ++c) {
+        run += work[c * E + e];
+        work[c * E + e] = run;
+    }
+}
+
+// ------------------------------------------------------------------ routing, kernel 3
 // One CTA (512 threads) per chunk.  Expert e's rows start at
 //   off[e] + (pairs of expert e in earlier chunks) + (rank inside this chunk),
-// the rank being the number of earlier tokens of the chunk that chose e.
+// the rank being the number of earlier tokens of the chunk that chose e; the
+// running totals of kernel 2 give the earlier chunks' pairs (row chunk - 1)
+// and each expert's total (row nchunks - 1).
 __global__ void __launch_bounds__(512) route_positions_kernel(const int32_t* __restrict__ idx, int64_t T, int E,
                                                               int k, const int32_t* __restrict__ work,
                                                               int64_t nchunks, int32_t* __restrict__ off,
@@ -109,14 +138,8 @@ __global__ void __launch_bounds__(512) route_positions_kernel(const int32_t* __r
     const int64_t chunk = blockIdx.x;
 
     for (int e = tid; e < E; e += blockDim.x) {
-        int total = 0, before = 0;
-        for (int64_t c = 0; c < nchunks; ++c) {
-            const int v = __ldg(work + c * E + e);
-            total += v;
-            if (c < chunk) before += v;
-        }
-        scan[e] = total;
-        base[e] = before;
+        scan[e] = __ldg(work + (nchunks - 1) * E + e);
+        base[e] = chunk > 0 ? __ldg(work + (chunk - 1) * E + e) : 0;
         mask[e] = 0ull;
     }
     __syncthreads();
@@ -316,6 +339,8 @@ extern "C" int fp8_moe_route_topk(const float* logits, int64_t T, int E, int top
     else if (epl <= 16) route_topk_kernel<16><<<g, 256, 0, s>>>(logits, T, E, topk, idx, gate, work);
     else route_topk_kernel<32><<<g, 256, 0, s>>>(logits, T, E, topk, idx, gate, work);
     if (cudaGetLastError() != cudaSuccess) return FP8_ERR_CUDA;
+    route_chunk_scan_kernel<<<unsigned((E + 255) / 256), 256, 0, s>>>(work, nchunks, E);
+    if (cudaGetLastError() != cudaSuccess) return FP8_ERR_CUDA;
     route_positions_kernel<<<g, 512, 0, s>>>(idx, T, E, topk, work, nchunks, expert_offsets, src_row, pos);
     return cudaGetLastError() == cudaSuccess ? FP8_OK : FP8_ERR_CUDA;
 }
@@ -362,7 +387,7 @@ extern "C" int fp8_moe_combine_bf16(const uint16_t* y, int64_t rows, const int32
 // file-scope device array instead of a caller buffer; every GPU that loads
 // the library keeps it (1 MiB) until the process exits.  No element needs to
 // start at zero: the first kernel writes all nchunks x E counts before the
-// second kernel reads any of them, in the same call.  Calls share the array,
+// later kernels of the same call read any of them.  Calls share the array,
 // so two calls whose kernels overlap on the GPU race on it.
 namespace fp8bs {
 static __device__ __align__(256) int32_t g_route_scratch[FP8_ROUTE_NOALLOC_MAX_WORK];
@@ -371,7 +396,9 @@ constexpr int kMaxDevices = 64;
 
 // Device address of g_route_scratch for the current device.  In host code
 // the array's name is only a host-side stand-in, so the address comes from
-// cudaGetSymbolAddress, once per device, with that device current.
+// cudaGetSymbolAddress, once per device, with that device current.  The
+// cached address belongs to the device's primary context: after a
+// cudaDeviceReset of that device it is stale, and the cache is not cleared.
 static int32_t* route_scratch_address() {
     static std::mutex mu;
     static int32_t* addr[kMaxDevices] = {};

@@ -365,7 +365,10 @@ FP8_API int fp8_moe_route_topk(const float* logits, int64_t T, int E, int topk,
  *     nothing.
  *   - The first call on a device looks up the array's device address
  *     (cudaGetSymbolAddress, with that device current) and caches it; make
- *     that first call before any stream capture.
+ *     that first call before any stream capture.  The cached address belongs
+ *     to the device's primary context: it is not valid after a
+ *     cudaDeviceReset of that device, and the library does not clear it, so
+ *     do not use this call on a device after resetting it.
  *   - Every call uses the same array and leaves its last contents there
  *     (nothing in it needs clearing: each call writes every word it reads).
  *     Calls whose kernels overlap on the GPU, e.g. on two streams at once,

@@ -39,7 +39,8 @@ def test_route_small_with_ties(fb, orc):
     _check_route(fb, orc, logits, 3)
 
 
-@pytest.mark.parametrize("T,E,k", [(1, 4, 4), (63, 33, 5), (65, 64, 8), (130, 1024, 32), (4096, 256, 8)])
+@pytest.mark.parametrize("T,E,k", [(1, 4, 4), (63, 33, 5), (65, 64, 8), (130, 1024, 32), (4096, 256, 8),
+                                   (20000, 256, 8), (65536, 256, 8)])
 def test_route_shapes(fb, orc, T, E, k):
     logits = torch.randn((T, E), generator=torch.Generator().manual_seed(T + E))
     _check_route(fb, orc, logits, k)
