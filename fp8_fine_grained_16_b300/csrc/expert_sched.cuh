@@ -1,6 +1,6 @@
 // expert_sched.cuh -- per-expert tile lists of the grouped (MoE) GEMMs.
 //
-// Expert e owns rows [off[e], off[e+1]) of A and D (page 4: each token's
+// Expert e owns rows [off[e], off[e+1]) of A and D (the jp-study.kr page: each token's
 // rows are dispatched to its routed experts).  A tile covers tile_rows rows
 // (256 for a CTA pair, 128 for one CTA), so expert e needs
 // ceil(rows_e / tile_rows) row tiles, each crossed with every column tile of

@@ -1,9 +1,9 @@
 // gemm_mx.cu -- block-scaled FP8 GEMM with the scales applied by the tensor
 // core, for power-of-two scales.
 //
-// Page 3 (gnrental.net) notes that the fine-grained tiles match the idea of
-// microscaling formats, which Blackwell tensor cores support; page 2
-// (tmdrlife.com) asks for tensor cores that take the scaling factors
+// The gnrental.net page notes that the fine-grained tiles match the idea of
+// microscaling formats, which Blackwell tensor cores support; tmdrlife.com page
+//  asks for tensor cores that take the scaling factors
 // themselves, and fixes some activation scales to integral powers of two.
 // With power-of-two scales (the quantisers' FP8_SCALE_POW2 mode) every scale
 // s = 2^e is exactly a UE8M0 scale factor, so the block-scaled tcgen05 MMA

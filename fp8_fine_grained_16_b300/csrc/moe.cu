@@ -1,6 +1,6 @@
-// moe.cu -- the MoE pieces around the grouped GEMM on one GPU (page 4: 256
+// moe.cu -- the MoE pieces around the grouped GEMM on one GPU (the jp-study.kr page: 256
 // routed experts, 8 active per token, activations quantised to FP8 before
-// dispatch; page 3: the combine stays in BF16).
+// dispatch; the gnrental.net page: the combine stays in BF16).
 //
 //   routing   top-k of each token's logits (ties to the lower expert),
 //             softmax gates over the selected logits, and a stable

@@ -1,6 +1,6 @@
-// quant.cu -- online max-abs E4M3 quantisers (page 4: the max-abs value is
+// quant.cu -- online max-abs E4M3 quantisers (the jp-study.kr page: the max-abs value is
 // computed online for each 1x128 activation tile and each 128x128 weight
-// block; page 2: each quantiser reads the BF16 values once and writes FP8
+// block; the tmdrlife.com page: each quantiser reads the BF16 values once and writes FP8
 // codes plus scales back in the same pass).
 //
 // All three kernels are HBM-bound streaming passes: 2 bytes read + 1 byte

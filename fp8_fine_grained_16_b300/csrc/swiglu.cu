@@ -1,6 +1,6 @@
 // swiglu.cu -- SwiGLU fused with 1x128 quantisation of its output, the input
-// of the MoE down-projection (page 2: the scaling factors of this activation
-// are integral powers of 2; page 4: quantisation is per 1x128 tile).
+// of the MoE down-projection (the tmdrlife.com page: the scaling factors of this activation
+// are integral powers of 2; the jp-study.kr page: quantisation is per 1x128 tile).
 //
 //   h[r][j] = SiLU(g) * u,  g = y[r][j], u = y[r][I + j],  SiLU(g) = g / (1 + e^-g)
 //

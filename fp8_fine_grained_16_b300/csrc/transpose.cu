@@ -1,6 +1,7 @@
 // transpose.cu -- transposed copy of a 128x128-block-quantised E4M3 matrix,
-// for FP8 Dgrad (page 1: E4M3 on all tensors, Fprop, Dgrad and Wgrad; page 4:
-// weights are quantised per 128x128 block).
+// for FP8 Dgrad (the why-be.why-be.co.kr (wr_id 35533) page: E4M3 for every
+// tensor, in Fprop, Dgrad and Wgrad; the jp-study.kr page: weights are
+// quantised per 128x128 block).
 //
 // The amax of a 128x128 block does not change when the block is transposed,
 // so quantising W^T per 128x128 block gives exactly the transposed codes and

@@ -3,14 +3,15 @@
  * block-scaled FP8 GEMMs on one B300 GPU (sm_103a).
  *
  * The method comes from five scraped web pages that restate DeepSeek-V3's FP8
- * training recipe.  They are cited as:
- *   page 1  (why-be.why-be.co.kr, wr_id 35533)  E4M3 on all tensors
- *   page 2  (tmdrlife.com, wr_id 13334)          limited-width accumulation,
+ * training recipe.  They have no titles; each is cited by its host, with the
+ * passage it gives:
+ *   why-be.why-be.co.kr (wr_id 35533) page   E4M3 for every tensor
+ *   tmdrlife.com page (wr_id 13334)          limited-width accumulation,
  *           promotion of partial sums into FP32, power-of-2 scales, the HBM
  *           round trip of quantised activations
- *   page 3  (gnrental.net, wr_id 40936)          promotion ("Figure 7 (b)"),
- *           BF16 combine, microscaling
- *   page 4  (jp-study.kr, document_srl 258368)   online max-abs per 1x128
+ *   gnrental.net page (wr_id 40936)          promotion ("Figure 7 (b)"), BF16
+ *           combine, microscaling
+ *   jp-study.kr page (document_srl 258368)   online max-abs per 1x128
  *           activation tile / 128x128 weight block, quantise before MoE
  *           dispatch, 256 routed experts with 8 active, 128-element
  *           accumulation interval, FP8 Wgrad ("Figure 6")
@@ -66,7 +67,7 @@ enum fp8_status {
 };
 
 /* flags of the quantisers */
-#define FP8_SCALE_POW2 1u     /* scales are exact powers of two (pages 2/3) */
+#define FP8_SCALE_POW2 1u     /* scales are exact powers of two (the tmdrlife.com and gnrental.net pages) */
 
 /* b_scale_mode of fp8_gemm_blockscaled */
 #define FP8_BSCALE_BLOCK128 0 /* sB [N/128][K/128]: one scale per 128x128 block */
@@ -77,15 +78,16 @@ enum fp8_status {
 #define FP8_OUT_F32 1
 
 /* ------------------------------------------------------------------------
- * Element-wise E4M3 cast (page 1: E4M3 on all tensors).
+ * Element-wise E4M3 cast (the why-be.why-be.co.kr (wr_id 35533) page: E4M3
+ * for every tensor).
  * q[i] = E4M3(x[i]) with round-to-nearest-even and saturation to +-448; the
  * same conversion every quantiser uses.  x: n fp32, q: n bytes.  n >= 0.
  * ---------------------------------------------------------------------- */
 FP8_API int fp8_cast_e4m3(const float* x, int64_t n, uint8_t* q, fp8_stream_t stream);
 
 /* ------------------------------------------------------------------------
- * 1x128 activation quantiser (page 4: max-abs computed online for each
- * 1x128 activation tile; page 2: one pass reads the BF16 values and writes
+ * 1x128 activation quantiser (the jp-study.kr page: max-abs computed online for each
+ * 1x128 activation tile; the tmdrlife.com page: one pass reads the BF16 values and writes
  * the FP8 codes back to HBM).
  * For each row m and K block kb, amax = max |x[m][128kb .. 128kb+127]|,
  * floored at 2^-64.  Default: s = amax/448 and inv = 448/amax (fp32
@@ -101,7 +103,7 @@ FP8_API int fp8_quant_act_1x128(const uint16_t* x, int64_t M, int64_t K, int64_t
                                 uint8_t* q, float* s, uint32_t flags, fp8_stream_t stream);
 
 /* ------------------------------------------------------------------------
- * 128x1 activation quantiser for Wgrad, output transposed (page 4: the
+ * 128x1 activation quantiser for Wgrad, output transposed (the jp-study.kr page: the
  * Wgrad operation runs in FP8).  Tiles run along tokens: for each column h
  * and token block tb, amax over x[128tb .. 128tb+127][h]; scale rule as
  * above.  The codes are written transposed so that tokens (the K dimension
@@ -115,7 +117,7 @@ FP8_API int fp8_quant_act_128x1(const uint16_t* x, int64_t T, int64_t H, int64_t
                                 uint8_t* qT, float* s, uint32_t flags, fp8_stream_t stream);
 
 /* ------------------------------------------------------------------------
- * 128x128 weight quantiser (page 4: max-abs computed online for each
+ * 128x128 weight quantiser (the jp-study.kr page: max-abs computed online for each
  * 128x128 weight block).  One scale per block; scale rule as above.
  *   w  bf16 [N][ldw] (K columns used), ldw >= K, ldw % 8 == 0
  *   q  E4M3 [N][K]
@@ -129,8 +131,8 @@ FP8_API int fp8_quant_weight_128x128(const uint16_t* w, int64_t N, int64_t K, in
 
 /* ------------------------------------------------------------------------
  * SwiGLU fused with 1x128 quantisation of its output: the input of the MoE
- * down-projection (page 2: that activation's scaling factors are integral
- * powers of 2, so flags = FP8_SCALE_POW2 is its natural setting; page 4:
+ * down-projection (the tmdrlife.com page: that activation's scaling factors are integral
+ * powers of 2, so flags = FP8_SCALE_POW2 is its natural setting; the jp-study.kr page:
  * 1x128 tiles).  For each row r and column j < I:
  *   h = (g * sigma(g)) * u,  g = y[r][j], u = y[r][I + j],
  *   sigma(g) = 1 / (1 + e^-g)
@@ -148,9 +150,9 @@ FP8_API int fp8_swiglu_quant_1x128(const uint16_t* y, int64_t R, int64_t I, int6
                                    uint8_t* q, float* s, uint32_t flags, fp8_stream_t stream);
 
 /* ------------------------------------------------------------------------
- * Block-scaled FP8 GEMM (pages 2 and 3: partial sums are accumulated on the
+ * Block-scaled FP8 GEMM (the tmdrlife.com and gnrental.net pages: partial sums are accumulated on the
  * tensor cores over a K interval, then multiplied by the scaling factors and
- * added into FP32; page 4: the interval is 128 elements).
+ * added into FP32; the jp-study.kr page: the interval is 128 elements).
  *   D[m][n] = sum_kb  sA[kb][m] * sB(n,kb) * P_kb[m][n],
  *   P_kb[m][n] = sum_{k in block kb} A[m][k] * B[n][k]   (E4M3 values)
  * P_kb is formed by tcgen05 MMAs into tensor memory; the outer sum runs in
@@ -227,7 +229,7 @@ FP8_API int fp8_gemm_blockscaled_ws(const uint8_t* a, const float* sa,
                                     void* workspace, int64_t workspace_bytes, fp8_stream_t stream);
 
 /* ------------------------------------------------------------------------
- * The block-scaled GEMM with its result quantised in the epilogue (page 2:
+ * The block-scaled GEMM with its result quantised in the epilogue (the tmdrlife.com page:
  * BF16 activations are read from HBM, quantised and written back, only to
  * be read again for the next MMA; quantising the producer's output where it
  * is formed removes that round trip).  D is computed exactly as by
@@ -258,9 +260,9 @@ FP8_API int fp8_gemm_blockscaled_q8_ws(const uint8_t* a, const float* sa,
 
 /* ------------------------------------------------------------------------
  * The same GEMM for power-of-two scales (the quantisers' FP8_SCALE_POW2
- * mode; page 2: integral-power-of-2 scaling factors), with the scales applied
- * by the tensor core (page 3: fine-grained tiles match microscaling, which
- * Blackwell tensor cores support; page 2: tensor cores that take the scaling
+ * mode; the tmdrlife.com page: integral-power-of-2 scaling factors), with the scales applied
+ * by the tensor core (the gnrental.net page: fine-grained tiles match microscaling, which
+ * Blackwell tensor cores support; the tmdrlife.com page: tensor cores that take the scaling
  * factors).  Each scale 2^e becomes a UE8M0 scale factor of the block-scaled
  * tcgen05 MMA, repeated over the four 32-element K groups of its 128-element
  * K block, and D accumulates in fp32 in tensor memory over the whole K:
@@ -278,8 +280,8 @@ FP8_API int fp8_gemm_blockscaled_pow2(const uint8_t* a, const float* sa,
 
 /* ------------------------------------------------------------------------
  * The grouped (per-expert) GEMM for power-of-two scales, on the microscaled
- * MMA of fp8_gemm_blockscaled_pow2 (page 4: 256 routed experts, each
- * processing the rows dispatched to it; pages 2/3: power-of-two scales,
+ * MMA of fp8_gemm_blockscaled_pow2 (the jp-study.kr page: 256 routed experts, each
+ * processing the rows dispatched to it; the tmdrlife.com and gnrental.net pages: power-of-two scales,
  * tensor cores that take the scaling factors).  Arguments, layouts, limits
  * and the handling of bad offsets are those of fp8_grouped_gemm_blockscaled;
  * every scale read must be a positive normal power of two (FP8_ERR_SCALE in
@@ -293,8 +295,9 @@ FP8_API int fp8_grouped_gemm_blockscaled_pow2(const uint8_t* a, const float* sa,
 
 /* ------------------------------------------------------------------------
  * Transposed copy of a 128x128-block-quantised E4M3 matrix, for FP8 Dgrad
- * (page 1: E4M3 on all tensors, Dgrad included; page 4: weights quantised
- * per 128x128 block).  The amax of a 128x128 block is the same after
+ * (the why-be.why-be.co.kr (wr_id 35533) page: E4M3 for every tensor,
+ * Dgrad included; the jp-study.kr page: weights quantised per 128x128
+ * block).  The amax of a 128x128 block is the same after
  * transposition, so (qT, sT) is exactly what fp8_quant_weight_128x128 would
  * give for the transposed bf16 matrix.  Dgrad dX = dY * W is then
  * fp8_gemm_blockscaled(a = 1x128 codes of dY, b = qT, sb = sT,
@@ -307,7 +310,7 @@ FP8_API int fp8_transpose_128x128(const uint8_t* q, const float* s, int64_t N, i
                                   uint8_t* qT, float* sT, fp8_stream_t stream);
 
 /* ------------------------------------------------------------------------
- * Grouped (per-expert) block-scaled FP8 GEMM for MoE (page 4: 256 routed
+ * Grouped (per-expert) block-scaled FP8 GEMM for MoE (the jp-study.kr page: 256 routed
  * experts; each expert processes the rows dispatched to it).  Expert e owns
  * rows [off[e], off[e+1]) of a and d and multiplies them by its own B_e:
  *   d[r][n] = sum_kb sa[kb][r] * sb[e][n/128][kb] * P_kb(a[r], b[e][n])
@@ -329,7 +332,7 @@ FP8_API int fp8_grouped_gemm_blockscaled(const uint8_t* a, const float* sa,
                                          uint16_t* d, fp8_stream_t stream);
 
 /* ------------------------------------------------------------------------
- * MoE routing on one GPU (page 4: each token activates 8 of 256 routed
+ * MoE routing on one GPU (the jp-study.kr page: each token activates 8 of 256 routed
  * experts).  Top-k of each token's logits, ties going to the lower expert
  * index; gates = softmax over the k selected logits (fp32); dispatch order =
  * (token, slot) pairs stably sorted by expert.
@@ -380,7 +383,7 @@ FP8_API int fp8_moe_route_topk_noalloc(const float* logits, int64_t T, int E, in
                                        int32_t* src_row, int32_t* pos, fp8_stream_t stream);
 
 /* ------------------------------------------------------------------------
- * Dispatch on one GPU: gather FP8 rows and their scales (page 4: activations
+ * Dispatch on one GPU: gather FP8 rows and their scales (the jp-study.kr page: activations
  * are quantised before the MoE up-projection, then dispatched in FP8).
  *   q_out[p][:] = q[src_row[p]][:],  s_out[kb][p] = s[kb][src_row[p]]
  *   q [rows][K], s [K/128][rows], src_row int32 [out_rows] (values in
@@ -392,7 +395,7 @@ FP8_API int fp8_permute_rows(const uint8_t* q, const float* s, int64_t rows, int
                              uint8_t* q_out, float* s_out, fp8_stream_t stream);
 
 /* ------------------------------------------------------------------------
- * Combine kept in BF16 (page 3: forward and backward combine stay in BF16):
+ * Combine kept in BF16 (the gnrental.net page: forward and backward combine stay in BF16):
  *   out[t][n] = bf16( sum_{j < topk} gate[t][j] * y[pos[t][j]][n] )
  * summed in fp32 in slot order, rounded to nearest-even once.
  *   y bf16 [rows][N], pos int32 [T][topk] (values in [0, rows)),

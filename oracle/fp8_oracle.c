@@ -6,16 +6,20 @@
  * baseline leg use it.  It shares no code, header, table or constant
  * generator with the CUDA library.
  *
- * Sources (the five scraped web pages on DeepSeek-V3's FP8 training; cited
- * by page number and host, then by the paragraph's subject):
- *   p1  why-be.why-be.co.kr wr_id=35533  -- "E4M3 on all tensors" paragraph
- *   p2  tmdrlife.com wr_id=13334         -- accumulation / promotion paragraphs,
- *                                          "integral power of 2" scaling paragraph
- *   p3  gnrental.net wr_id=40936         -- BF16 combine, promotion ("Figure 7 (b)")
- *   p4  jp-study.kr document_srl=258368  -- online max-abs per 1x128 / 128x128,
- *                                          quantise before MoE dispatch, 256
- *                                          routed experts / top-8, 128-element
- *                                          accumulation interval, FP8 Wgrad
+ * Sources: the five scraped web pages on DeepSeek-V3's FP8 training.  They
+ * have no titles; each is cited by its host, then by the passage's subject:
+ *   why-be.why-be.co.kr (wr_id 35533) page -- the format passage (E4M3 for
+ *                                            every tensor)
+ *   tmdrlife.com page (wr_id 13334)        -- accumulation / promotion
+ *                                            passages, the power-of-2
+ *                                            scaling passage
+ *   gnrental.net page (wr_id 40936)        -- BF16 combine, promotion
+ *                                            ("Figure 7 (b)")
+ *   jp-study.kr page (document_srl 258368) -- online max-abs per 1x128 /
+ *                                            128x128, quantise before MoE
+ *                                            dispatch, 256 routed experts /
+ *                                            top-8, 128-element accumulation
+ *                                            interval, FP8 Wgrad
  *
  * Every routine is the plain definition written out; loops run in the
  * obvious order.  Floating point: fp32 where the method fixes fp32 (scales,
@@ -90,8 +94,9 @@ void orc_bf16_to_float(const uint16_t* h, int64_t n, float* out) {
 }
 
 /* ------------------------------------------------------------------ */
-/* O1  E4M3 codec (p1: E4M3 -- 4 exponent bits, 3 mantissa bits -- on    */
-/*     all tensors; bit layout per reading R1)                          */
+/* O1  E4M3 codec (why-be.why-be.co.kr 35533 page: E4M3 -- 4 exponent   */
+/*     bits, 3 mantissa bits -- for every tensor; bit layout per        */
+/*     reading R1)                                                      */
 /* ------------------------------------------------------------------ */
 
 /* value = (-1)^s * 2^(e-7) * (1 + m/8) for e > 0, (-1)^s * 2^-6 * m/8 for e = 0 */
@@ -142,9 +147,10 @@ void orc_e4m3_encode_bits(uint64_t start, int64_t n, uint8_t* q) {
 }
 
 /* ------------------------------------------------------------------ */
-/* O2  Tile scale (p4: max-abs computed online per 1x128 activation     */
-/*     tile / 128x128 weight block; p2, p3: scales that are integral    */
-/*     powers of 2 for some activations).  Readings R2, R3.            */
+/* O2  Tile scale (jp-study.kr page: max-abs computed online per 1x128  */
+/*     activation tile / 128x128 weight block; tmdrlife.com and         */
+/*     gnrental.net pages: scales that are integral powers of 2 for     */
+/*     some activations).  Readings R2, R3.                             */
 /* ------------------------------------------------------------------ */
 
 #define ORC_FLAG_POW2 1u
@@ -197,7 +203,7 @@ void orc_quant_act_1x128(const uint16_t* x, int64_t M, int64_t K, int64_t ldx,
 
 /* 1x128 tiles of an fp32 matrix: x fp32 [M][K], q [M][K], s [K/128][M].
  * The same tile rule as above on fp32 values; it defines the quantisation of
- * a GEMM result in the producer's epilogue (p2: quantising where the BF16
+ * a GEMM result in the producer's epilogue (tmdrlife.com page: quantising where the BF16
  * activation is formed instead of re-reading it from HBM). */
 void orc_quant_act_1x128_f32(const float* x, int64_t M, int64_t K, uint8_t* q, float* s, uint32_t flags) {
     int64_t nkb = K / 128;
@@ -219,8 +225,8 @@ void orc_quant_act_1x128_f32(const float* x, int64_t M, int64_t K, uint8_t* q, f
 
 /* ------------------------------------------------------------------ */
 /* SwiGLU fused with 1x128 quantisation of its output (the MoE         */
-/* down-projection input; p2: that activation's scales are integral    */
-/* powers of 2)                                                         */
+/* down-projection input; tmdrlife.com page: that activation's scales  */
+/* are integral powers of 2)                                            */
 /* ------------------------------------------------------------------ */
 
 /* e^x in fp32 by the published Cody-Waite method: x = n*ln2 + r with
@@ -335,9 +341,10 @@ void orc_quant_weight_128x128(const uint16_t* w, int64_t N, int64_t K, int64_t l
 }
 
 /* ------------------------------------------------------------------ */
-/* O4  Block-scaled GEMM (p2, p3: each K interval is accumulated, then  */
-/*     multiplied by its scaling factors and added into FP32; p4: the  */
-/*     interval is 128 elements).  D[m][n] = sum_k A^[m][k] * B^[n][k]   */
+/* O4  Block-scaled GEMM (tmdrlife.com and gnrental.net pages: each K  */
+/*     interval is accumulated, then multiplied by its scaling factors  */
+/*     and added into FP32; jp-study.kr page: the interval is 128       */
+/*     elements).  D[m][n] = sum_k A^[m][k] * B^[n][k]                 */
 /*     with A^ = decode(qA) * sA and B^ = decode(qB) * sB, both exact   */
 /*     in fp64.  The sum runs over k ascending in fp64.                 */
 /*     b_mode 0: sB [N/128][K/128] (128x128 blocks)                     */
@@ -392,8 +399,9 @@ void orc_gemm_blockscaled(const uint8_t* a, const float* sa, const uint8_t* b, c
 }
 
 /* ------------------------------------------------------------------ */
-/* O5  MoE routing and grouped GEMM (p4: 256 routed experts, 8 active   */
-/*     per token; activations quantised before dispatch).  Reading R5. */
+/* O5  MoE routing and grouped GEMM (jp-study.kr page: 256 routed       */
+/*     experts, 8 active per token; activations quantised before        */
+/*     dispatch).  Reading R5.                                          */
 /* ------------------------------------------------------------------ */
 
 /* logits fp32 [T][E] -> idx int32 [T][k], gate fp32 [T][k],
@@ -483,9 +491,10 @@ void orc_grouped_gemm_at(const uint8_t* a, const float* sa, const uint8_t* b, co
 }
 
 /* ------------------------------------------------------------------ */
-/* O6  Combine, kept in BF16 (p3: forward and backward combine stay in  */
-/*     BF16): out[t][n] = sum_j gate[t][j] * y[pos[t][j]][n], summed in  */
-/*     slot order in fp64, rounded to bf16 once.                        */
+/* O6  Combine, kept in BF16 (gnrental.net page: forward and backward   */
+/*     combine stay in BF16): out[t][n] = sum_j gate[t][j] *           */
+/*     y[pos[t][j]][n], summed in slot order in fp64, rounded to bf16   */
+/*     once.                                                            */
 /* ------------------------------------------------------------------ */
 
 void orc_moe_combine(const uint16_t* y, const int32_t* pos, const float* gate,

@@ -1,6 +1,6 @@
 """GPU parity of the block-scaled FP8 GEMM against the oracle's fp64 product
-of the same E4M3 operands and scales (pages 2/3: per-interval promotion into
-FP32 scaled by the two scales; page 4: 128-element interval)."""
+of the same E4M3 operands and scales (the tmdrlife.com and gnrental.net pages: per-interval promotion into
+FP32 scaled by the two scales; the jp-study.kr page: 128-element interval)."""
 import numpy as np
 import pytest
 import torch
@@ -173,7 +173,7 @@ def test_gemm_repeat_runs_bit_identical(fb, M, N, K, mode):
 
 def test_tensor_core_accumulation_precision_probe(fb, orc):
     """How many bits the tcgen05 E4M3 accumulation keeps inside one 128-element
-    K block (pages 2 and 4: Hopper's limited accumulation width is why partial
+    K block (the tmdrlife.com and jp-study.kr pages: Hopper's limited accumulation width is why partial
     sums are promoted every 128 elements; nothing on the pages fixes it for
     this part, so this is a measurement, printed, with a floor).
 

@@ -2,8 +2,8 @@
 tensor core as UE8M0 microscaling factors) against the oracle's fp64 product
 of the same E4M3 operands and scales.
 
-Page 2 (tmdrlife.com) fixes some activation scales to integral powers of 2
-and asks for tensor cores that accept the scaling factors; page 3
+The tmdrlife.com page fixes some activation scales to integral powers of 2
+and asks for tensor cores that accept the scaling factors; the gnrental.net page
 (gnrental.net) ties the fine-grained tiles to the microscaling formats of
 Blackwell tensor cores.  With power-of-two scales the block-promoted sum of
 the pages and the microscaled sum are the same real number before rounding,

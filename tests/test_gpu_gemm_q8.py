@@ -1,5 +1,5 @@
 """GPU parity of the GEMM whose epilogue quantises D per 1x128 tile along N
-(page 2: the BF16 output of one operator is written to HBM, read back and
+(the tmdrlife.com page: the BF16 output of one operator is written to HBM, read back and
 quantised, and read again for the next MMA; quantising it where it is formed
 removes that round trip).
 

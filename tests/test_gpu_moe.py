@@ -1,6 +1,6 @@
 """GPU parity of routing, dispatch (permute), the grouped GEMM and the BF16
-combine (page 4: 256 routed experts, 8 active, activations quantised before
-dispatch; page 3: combine kept in BF16)."""
+combine (the jp-study.kr page: 256 routed experts, 8 active, activations quantised before
+dispatch; the gnrental.net page: combine kept in BF16)."""
 import numpy as np
 import pytest
 import torch

@@ -1,6 +1,6 @@
 """GPU parity of the grouped (per-expert) GEMM for power-of-two scales on the
-microscaled tensor-core MMA (page 4: 256 routed experts, each processing the
-rows dispatched to it; pages 2/3: power-of-two scales, tensor cores that take
+microscaled tensor-core MMA (the jp-study.kr page: 256 routed experts, each processing the
+rows dispatched to it; the tmdrlife.com and gnrental.net pages: power-of-two scales, tensor cores that take
 the scaling factors) against the oracle's fp64 per-expert product: the GEMM
 tolerance plus the element-wise recursive-summation bound of the dense
 power-of-two tests (2 * (K + K/32) * 2^-24 * sum|a*b| + one bf16 rounding).

@@ -1,7 +1,7 @@
 """GPU parity of the E4M3 cast and the three quantisers against the oracle:
-codes and scales must match bit for bit (page 4: online max-abs per 1x128
-activation tile and per 128x128 weight block; page 4: FP8 Wgrad -> 128x1
-tiles along tokens; pages 2/3: power-of-2 scales)."""
+codes and scales must match bit for bit (the jp-study.kr page: online max-abs per 1x128
+activation tile and per 128x128 weight block; the jp-study.kr page: FP8 Wgrad -> 128x1
+tiles along tokens; the tmdrlife.com and gnrental.net pages: power-of-2 scales)."""
 import numpy as np
 import pytest
 import torch

@@ -1,5 +1,6 @@
-"""Pins for the oracle's E4M3 codec (format: page 1, "E4M3 on all tensors";
-bit layout, rounding and saturation per the E4M3FN reading)."""
+"""Pins for the oracle's E4M3 codec.  The why-be.why-be.co.kr (wr_id 35533)
+page fixes the format (E4M3 for every tensor); the bit layout, rounding and
+saturation follow the E4M3FN reading."""
 import ctypes
 import math
 

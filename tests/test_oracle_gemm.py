@@ -1,6 +1,6 @@
-"""Pins for the oracle's block-scaled GEMM (pages 2/3: each 128-element K
+"""Pins for the oracle's block-scaled GEMM (the tmdrlife.com and gnrental.net pages: each 128-element K
 interval is accumulated, multiplied by the scaling factors and added into
-FP32; page 4: the interval is 128 elements).  The oracle forms the exact
+FP32; the jp-study.kr page: the interval is 128 elements).  The oracle forms the exact
 fp64 product of the dequantised operands, which equals the block-promoted
 sum sum_kb sA*sB*P_kb."""
 from fractions import Fraction

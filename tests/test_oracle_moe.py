@@ -1,5 +1,5 @@
-"""Pins for the oracle's MoE pieces (page 4: 256 routed experts, 8 active per
-token; activations quantised to FP8 before dispatch; page 3: combine kept in
+"""Pins for the oracle's MoE pieces (the jp-study.kr page: 256 routed experts, 8 active per
+token; activations quantised to FP8 before dispatch; the gnrental.net page: combine kept in
 BF16).  Routing order and gates follow the stated readings."""
 import itertools
 import math

@@ -1,6 +1,6 @@
-"""Pins for the oracle's quantisers (page 4: max-abs taken online per 1x128
-activation tile and per 128x128 weight block; pages 2/3: integral power-of-2
-scales for some activations; page 4: Wgrad runs in FP8, which needs 128x1
+"""Pins for the oracle's quantisers (the jp-study.kr page: max-abs taken online per 1x128
+activation tile and per 128x128 weight block; the tmdrlife.com and gnrental.net pages: integral power-of-2
+scales for some activations; the jp-study.kr page: Wgrad runs in FP8, which needs 128x1
 tiles along tokens)."""
 import math
 import os

@@ -1,5 +1,5 @@
 """Pins for the oracle's SwiGLU + 1x128 quantisation (the MoE down-projection
-input; page 2 fixes that activation's scales to integral powers of 2).
+input; the tmdrlife.com page fixes that activation's scales to integral powers of 2).
 
 SwiGLU(g, u) = SiLU(g) * u with SiLU(g) = g / (1 + e^-g).  The oracle forms
 it in fp32 steps with its own e^x (Cody-Waite reduction, degree-7 Taylor), so
