@@ -351,12 +351,14 @@ class _SmClock:
     def __init__(self):
         self.h = None
         self.last = None
+        self.index = torch.cuda.current_device()
         try:
             import pynvml
             pynvml.nvmlInit()
             self.nv = pynvml
-            self.h = pynvml.nvmlDeviceGetHandleByIndex(torch.cuda.current_device())
-        except Exception:
+            self.h = pynvml.nvmlDeviceGetHandleByIndex(self.index)
+        except Exception as e:               # fall back to one nvidia-smi query per row
+            sys.stderr.write("NVML unavailable (%s); row clocks from nvidia-smi\n" % e)
             self.h = None
 
     def read(self):
@@ -364,6 +366,17 @@ class _SmClock:
             return None
         try:
             return float(self.nv.nvmlDeviceGetClockInfo(self.h, self.nv.NVML_CLOCK_SM))
+        except Exception as e:
+            sys.stderr.write("NVML clock read failed (%s); row clocks from nvidia-smi\n" % e)
+            self.h = None
+            return None
+
+    def query(self):
+        """One nvidia-smi reading of the SM clock (MHz), or None."""
+        try:
+            out = subprocess.run(["nvidia-smi", "-i", str(self.index), "--query-gpu=clocks.sm",
+                                  "--format=csv,noheader,nounits"], capture_output=True, text=True, timeout=10)
+            return float(out.stdout.strip().splitlines()[0])
         except Exception:
             return None
 
@@ -391,7 +404,7 @@ def _time(fn, reps, warm, flush, stream):
         c = _SM_CLOCK.read()
         if c is not None:
             mhz.append(c)
-    _SM_CLOCK.last = statistics.median(mhz) if mhz else None
+    _SM_CLOCK.last = statistics.median(mhz) if mhz else _SM_CLOCK.query()
     return statistics.median(ts)
 
 

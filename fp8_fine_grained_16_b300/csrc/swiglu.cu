@@ -38,10 +38,10 @@ FP8_DEV float2 one_plus_exp(float2 x) {
     // float -> integer conversions.
     const float2 big = __fadd2_rn(t, make_float2(0x1.8p23f, 0x1.8p23f));
     const float2 n = __fadd2_rn(big, make_float2(-0x1.8p23f, -0x1.8p23f));
-    const int nx = __float_as_int(big.x) - 0x4B400000, ny = __float_as_int(big.y) - 0x4B400000;
-    const float2 mn = make_float2(-n.x, -n.y);
-    float2 r = __ffma2_rn(mn, make_float2(0x1.62e4p-1f, 0x1.62e4p-1f), xc);        // ln2, high part (exact product)
-    r = __ffma2_rn(mn, make_float2(0x1.7f7d1cp-20f, 0x1.7f7d1cp-20f), r);          // ln2, low part
+    // r = x - n*ln2 in two steps; n * (-c) is exactly -(n * c), so each fused
+    // step rounds the same value as with -n
+    float2 r = __ffma2_rn(n, make_float2(-0x1.62e4p-1f, -0x1.62e4p-1f), xc);      // ln2, high part (exact product)
+    r = __ffma2_rn(n, make_float2(-0x1.7f7d1cp-20f, -0x1.7f7d1cp-20f), r);        // ln2, low part
     float2 p = make_float2(0x1.a01a02p-13f, 0x1.a01a02p-13f);                      // 1/7!
     p = __ffma2_rn(p, r, make_float2(0x1.6c16c2p-10f, 0x1.6c16c2p-10f));            // 1/6!
     p = __ffma2_rn(p, r, make_float2(0x1.111112p-7f, 0x1.111112p-7f));              // 1/5!
@@ -50,8 +50,11 @@ FP8_DEV float2 one_plus_exp(float2 x) {
     p = __ffma2_rn(p, r, make_float2(0.5f, 0.5f));
     p = __ffma2_rn(p, r, make_float2(1.0f, 1.0f));
     p = __ffma2_rn(p, r, make_float2(1.0f, 1.0f));
-    const float2 e = __fmul2_rn(p, make_float2(__int_as_float((nx + 127) << 23),       // 2^n, n in [-126, 127]
-                                                __int_as_float((ny + 127) << 23)));
+    // 2^n, n in [-126, 127]: the sum's bits are 0x4B400000 + n, so its bits
+    // shifted up by 23 (0x4B400000 << 23 vanishes mod 2^32) plus 127 << 23
+    // are those of 2^n
+    const float2 e = __fmul2_rn(p, make_float2(__int_as_float((__float_as_int(big.x) << 23) + (127 << 23)),
+                                                __int_as_float((__float_as_int(big.y) << 23) + (127 << 23))));
     const float inf = __int_as_float(0x7F800000);
     return __fadd2_rn(make_float2(1.0f, 1.0f), make_float2(x.x > 88.0f ? inf : e.x, x.y > 88.0f ? inf : e.y));
 }

@@ -13,10 +13,15 @@
 // loads the 16-byte pieces at byte column 16s of the input rows 4q .. 4q+3
 // (s = l % 8, q = 4w + l / 8): every load instruction of a warp reads four
 // whole 128-byte rows.  Each of its four 4x4 byte blocks is transposed in
-// registers (byte permutes) and lands in a shared tile whose word index is
-// rotated per output row c by (c/4 + 4*(c%4)) mod 32, which keeps both the
-// stores (slot q + 4s + const: 32 distinct banks per warp) and the loads (a
-// warp reads 16 consecutive rows, two threads per row) conflict-free; the
+// registers (byte permutes) and lands in a shared tile whose words are
+// rotated per output row c by rot(c) = 4 * ((c + c/16) mod 8) words.  The
+// stores are conflict-free (for a store instruction c/16 = s and c mod 8 is
+// fixed, so slot q + 4 * ((k + s) mod 8) takes 32 distinct banks), and since
+// the rotation is a multiple of four words the loads are aligned 16-byte
+// pieces, also conflict-free (the eight threads of a load phase read four
+// consecutive rows, two halves each, whose rotations differ by one piece and
+// whose halves by four): four loads per thread instead of sixteen, which
+// relieves the shared-memory instruction queue that throttled the copy.  The
 // output leaves as 16-byte pieces of whole 128-byte rows.
 #include "common.cuh"
 
@@ -40,8 +45,9 @@ __global__ void __launch_bounds__(256) transpose_128x128_kernel(const uint8_t* _
                                                                 int64_t K, uint8_t* __restrict__ qT,
                                                                 float* __restrict__ sT) {
     // T[c][slot]: output row c (= input column), 32 words = input rows 4*word ..
-    // 4*word+3; word `wd` of row c sits at slot (wd + c/4 + 4*(c%4)) % 32.
-    __shared__ uint32_t T[128 * 32];
+    // 4*word+3; word `wd` of row c sits at slot (wd + rot(c)) % 32.
+    __shared__ __align__(16) uint32_t T[128 * 32];
+    auto rot = [](int c) { return 4 * ((c + (c >> 4)) & 7); };
     const int64_t nkb = K >> 7, nnb = N >> 7;
     const int64_t nb = blockIdx.x / nkb, kb = blockIdx.x - nb * nkb;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -60,8 +66,8 @@ __global__ void __launch_bounds__(256) transpose_128x128_kernel(const uint8_t* _
             transpose4x4(in, out);
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
-                const int c = 16 * sg + 4 * w + i;         // input column = output row: c/4 = 4sg + w, c%4 = i
-                T[c * 32 + ((qd + 4 * sg + w + 4 * i) & 31)] = out[i];
+                const int c = 16 * sg + 4 * w + i;         // input column = output row
+                T[c * 32 + ((qd + rot(c)) & 31)] = out[i];
             }
         }
     }
@@ -70,15 +76,9 @@ __global__ void __launch_bounds__(256) transpose_128x128_kernel(const uint8_t* _
     const int c = threadIdx.x >> 1, h = threadIdx.x & 1;
     uint8_t* dst = qT + (kb * 128 + c) * N + nb * 128 + 64 * h;
 #pragma unroll
-    for (int v = 0; v < 4; ++v) {
-        uint32_t w[4];
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-            const int wd = 16 * h + 4 * v + e;
-            w[e] = T[c * 32 + ((wd + (c >> 2) + 4 * (c & 3)) & 31)];
-        }
-        reinterpret_cast<uint4*>(dst)[v] = make_uint4(w[0], w[1], w[2], w[3]);
-    }
+    for (int v = 0; v < 4; ++v)
+        reinterpret_cast<uint4*>(dst)[v] =
+            *reinterpret_cast<const uint4*>(&T[c * 32 + ((16 * h + 4 * v + rot(c)) & 31)]);
     if (threadIdx.x == 0) sT[kb * nnb + nb] = s[nb * nkb + kb];
 }
 
