@@ -774,8 +774,8 @@ CASES = ("dense", "wgrad", "wgrad_small", "q8", "dgrad_transpose", "quant_1x128"
 
 def run_case(name: str, reps: int):
     """One kernel of the path on a bounded synthetic case, launched 1 + reps
-    times (the first launch warms up): what an ncu capture of that kernel
-    runs (`-k <kernel> -s 1 -c 1`).  Random E4M3 codes (NaN codes excluded)
+    times (the first launch warms up; L2 is flushed before each timed one):
+    what an ncu capture of that kernel runs (`-k <kernel> -s 1 -c 1`).  Random E4M3 codes (NaN codes excluded)
     and log-uniform scales stand in for quantised operands; the grouped
     cases keep the MoE shapes with 32 experts of ~128 rows (Poisson) so a
     full-metric capture holds about 1 GB."""
@@ -873,11 +873,13 @@ def run_case(name: str, reps: int):
     else:
         raise SystemExit("unknown case %r (one of %s)" % (name, ", ".join(CASES)))
     st = torch.cuda.current_stream()
+    flush = L2Flush(dev)
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     fn()
     torch.cuda.synchronize()
     ts = []
     for _ in range(reps):
+        flush()
         e0.record(st)
         fn()
         e1.record(st)
