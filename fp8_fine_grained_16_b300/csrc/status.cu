@@ -4,13 +4,15 @@
 extern "C" int fp8bs_gemm_take_status(cudaStream_t stream);
 extern "C" int fp8bs_moe_take_status(cudaStream_t stream);
 extern "C" int fp8bs_gemm_mx_take_status(cudaStream_t stream);
+extern "C" int fp8bs_transpose_take_status(cudaStream_t stream);
 
 extern "C" int fp8_get_status(fp8_stream_t stream) {
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     const int a = fp8bs_gemm_take_status(s);
     const int b = fp8bs_moe_take_status(s);
     const int c = fp8bs_gemm_mx_take_status(s);
-    return a != FP8_OK ? a : (b != FP8_OK ? b : c);
+    const int d = fp8bs_transpose_take_status(s);
+    return a != FP8_OK ? a : (b != FP8_OK ? b : (c != FP8_OK ? c : d));
 }
 
 extern "C" const char* fp8_strerror(int code) {

@@ -9,23 +9,37 @@
 // dX = dY * W, is then the block-scaled GEMM with A = dY (1x128 tiles) and
 // B = W^T from this copy.
 //
-// One CTA (256 threads) per 128x128 byte tile.  Thread (warp w, lane l)
-// loads the 16-byte pieces at byte column 16s of the input rows 4q .. 4q+3
-// (s = l % 8, q = 4w + l / 8): every load instruction of a warp reads four
-// whole 128-byte rows.  Each of its four 4x4 byte blocks is transposed in
-// registers (byte permutes) and lands in a shared tile whose words are
-// rotated per output row c by rot(c) = 4 * ((c + c/16) mod 8) words.  The
-// stores are conflict-free (for a store instruction c/16 = s and c mod 8 is
-// fixed, so slot q + 4 * ((k + s) mod 8) takes 32 distinct banks), and since
-// the rotation is a multiple of four words the loads are aligned 16-byte
-// pieces, also conflict-free (the eight threads of a load phase read four
-// consecutive rows, two halves each, whose rotations differ by one piece and
-// whose halves by four): four loads per thread instead of sixteen, which
-// relieves the shared-memory instruction queue that throttled the copy.  The
-// output leaves as 16-byte pieces of whole 128-byte rows.
+// A persistent kernel, one CTA per SM.  Warp 0 (one lane) streams the CTA's
+// 128x128-byte blocks into an 8-stage ring with TMA tensor loads (128-byte
+// swizzle: 16-byte piece j of tile row r sits at piece j ^ (r % 8)), so that
+// 128 KB of loads per SM stay in flight while the blocks before them are
+// transposed.  Each of four worker warps takes every fourth block: a thread
+// transposes two 16x16-byte sub-blocks (sixteen 16-byte shared loads, 4x4 byte
+// transposes in registers, sixteen 16-byte shared stores), writes them into the
+// warp's own output tile in the same swizzled layout, and one lane stores that
+// tile to W^T with a TMA tensor store (the warp copies its tiles' block
+// scales up front, one tile per lane).  Thread (lane l) of sub-block pass b
+// takes input piece column sx = l % 8 and input row group p = sx ^ (l / 8 + 4b):
+// the eight threads of each 16-byte access phase then have distinct sx and
+// distinct p, so both the swizzled loads (piece sx ^ (row % 8)) and stores
+// (piece p ^ (row % 8)) hit eight different 16-byte bank groups.
+//
+// Every wait is bounded; an expired wait records FP8_ERR_TIMEOUT, the warps
+// stop, and the producer lets its copies in flight land before the CTA exits.
 #include "common.cuh"
+#include "tensor_map.cuh"
 
 namespace fp8bs {
+
+__device__ int g_tr_status;
+FP8_DEV void tr_record(int code) { atomicCAS(&g_tr_status, 0, code); }
+
+constexpr int kTrStages = 8;                            // input ring depth (128x128-byte tiles)
+constexpr int kTrWorkers = 4;                           // transposing warps
+constexpr int kTrTile = 128 * 128;                      // bytes per tile
+constexpr int kTrThreads = 32 * (1 + kTrWorkers);
+constexpr int kTrBarOff = (kTrStages + kTrWorkers) * kTrTile;
+constexpr int kTrSmem = kTrBarOff + 2 * kTrStages * 8 + 16 + 1024;   // + barriers, abort flag, 1024-byte alignment
 
 // 4x4 byte transpose: in[r] holds bytes (r,0..3) little-endian; out[c] gets
 // bytes (0..3,c).
@@ -40,46 +54,136 @@ FP8_DEV void transpose4x4(const uint32_t (&in)[4], uint32_t (&out)[4]) {
     out[3] = __byte_perm(t2, t3, 0x7632);                    // a3 b3 c3 d3
 }
 
-__global__ void __launch_bounds__(256) transpose_128x128_kernel(const uint8_t* __restrict__ q,
-                                                                const float* __restrict__ s, int64_t N,
-                                                                int64_t K, uint8_t* __restrict__ qT,
-                                                                float* __restrict__ sT) {
-    // T[c][slot]: output row c (= input column), 32 words = input rows 4*word ..
-    // 4*word+3; word `wd` of row c sits at slot (wd + rot(c)) % 32.
-    __shared__ __align__(16) uint32_t T[128 * 32];
-    auto rot = [](int c) { return 4 * ((c + (c >> 4)) & 7); };
-    const int64_t nkb = K >> 7, nnb = N >> 7;
-    const int64_t nb = blockIdx.x / nkb, kb = blockIdx.x - nb * nkb;
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const uint8_t* src = q + (nb * 128) * K + kb * 128;
+// Tile t of the CTA's list: block (nb, kb) of the [N/128][K/128] grid, kb fastest.
+__global__ void __launch_bounds__(kTrThreads, 1) transpose_128x128_kernel(const __grid_constant__ CUtensorMap tmIn,
+                                                                          const __grid_constant__ CUtensorMap tmOut,
+                                                                          const float* __restrict__ s,
+                                                                          float* __restrict__ sT, int64_t nnb,
+                                                                          int64_t nkb) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint8_t* in_tiles = smem;
+    uint8_t* out_tiles = smem + kTrStages * kTrTile;
+    uint64_t* full = reinterpret_cast<uint64_t*>(smem + kTrBarOff);
+    uint64_t* empty = full + kTrStages;
+    volatile int* abort_s = reinterpret_cast<volatile int*>(empty + kTrStages);
 
-    {
-        const int sg = lane & 7, qd = 4 * warp + (lane >> 3);    // 16-byte column piece, input row quad
-        uint4 in4[4];
-#pragma unroll
-        for (int r = 0; r < 4; ++r)
-            in4[r] = __ldg(reinterpret_cast<const uint4*>(src + (4 * qd + r) * K) + sg);
-#pragma unroll
-        for (int w = 0; w < 4; ++w) {
-            const uint32_t in[4] = {(&in4[0].x)[w], (&in4[1].x)[w], (&in4[2].x)[w], (&in4[3].x)[w]};
-            uint32_t out[4];
-            transpose4x4(in, out);
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                const int c = 16 * sg + 4 * w + i;         // input column = output row
-                T[c * 32 + ((qd + rot(c)) & 31)] = out[i];
-            }
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int64_t ntiles = nnb * nkb;
+    const int64_t my_tiles = int64_t(blockIdx.x) < ntiles ? (ntiles - 1 - blockIdx.x) / gridDim.x + 1 : 0;
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < kTrStages; ++i) {
+            mbar_init(&full[i], 1);
+            mbar_init(&empty[i], 1);
         }
+        *abort_s = 0;
+        fence_mbar_init();
     }
     __syncthreads();
-    // output row c = t / 2, words 16h .. 16h+15 (h = t % 2), four 16-byte stores
-    const int c = threadIdx.x >> 1, h = threadIdx.x & 1;
-    uint8_t* dst = qT + (kb * 128 + c) * N + nb * 128 + 64 * h;
+
+    if (warp == 0) {
+        // ================= TMA producer
+        if (lane == 0) {
+            tma_prefetch_desc(&tmIn);
+            bool ok = true;
+            int64_t i = 0;
+            for (; i < my_tiles; ++i) {
+                const uint32_t st = uint32_t(i % kTrStages), ph = uint32_t(i / kTrStages) & 1u;
+                if (!mbar_wait_bounded(&empty[st], ph ^ 1u, abort_s)) { ok = false; break; }
+                const int64_t t = blockIdx.x + i * gridDim.x;
+                const int64_t nb = t / nkb, kb = t - nb * nkb;
+                mbar_arrive_expect_tx(&full[st], kTrTile);
+                tma_load_2d(in_tiles + st * kTrTile, &tmIn, &full[st], int32_t(kb * 128), int32_t(nb * 128));
+            }
+            if (!ok) {
+                tr_record(FP8_ERR_TIMEOUT);
+                // the copies already issued land before the CTA's shared memory goes away
+                int zero = 0;
+                for (int64_t j = i > kTrStages ? i - kTrStages : 0; j < i; ++j)
+                    mbar_wait_bounded(&full[j % kTrStages], uint32_t(j / kTrStages) & 1u,
+                                      reinterpret_cast<volatile int*>(&zero));
+            }
+        }
+        __syncwarp();
+        return;
+    }
+
+    // ================= worker warps
+    const int wk = warp - 1;
+    uint8_t* out = out_tiles + wk * kTrTile;
+    const int sx = lane & 7, tq = lane >> 3;
+    // the block scales of this warp's tiles first, one tile per lane: the
+    // loads are independent, so their latency is paid once per 32 tiles and
+    // overlaps the first tile's copy instead of stalling every tile
+    for (int64_t i = wk + int64_t(kTrWorkers) * lane; i < my_tiles; i += int64_t(kTrWorkers) * 32) {
+        const int64_t t = blockIdx.x + i * gridDim.x;
+        const int64_t nb = t / nkb, kb = t - nb * nkb;
+        sT[kb * nnb + nb] = s[nb * nkb + kb];
+    }
+    bool ok = true;
+    for (int64_t i = wk; i < my_tiles; i += kTrWorkers) {
+        const uint32_t st = uint32_t(i % kTrStages), ph = uint32_t(i / kTrStages) & 1u;
+        // every lane waits (acquiring the tile); the warp leaves together if any lane gave up
+        if (!__all_sync(0xFFFFFFFFu, mbar_wait_bounded(&full[st], ph, abort_s))) { ok = false; break; }
+        const uint8_t* in = in_tiles + st * kTrTile;
+        // the previous store out of this warp's output tile has finished reading it
+        if (lane == 0) bulk_wait_group_read0();
+        __syncwarp();
 #pragma unroll
-    for (int v = 0; v < 4; ++v)
-        reinterpret_cast<uint4*>(dst)[v] =
-            *reinterpret_cast<const uint4*>(&T[c * 32 + ((16 * h + 4 * v + rot(c)) & 31)]);
-    if (threadIdx.x == 0) sT[kb * nnb + nb] = s[nb * nkb + kb];
+        for (int b = 0; b < 2; ++b) {
+            const int p = sx ^ (tq + 4 * b);                  // input rows 16p .. 16p+15
+            uint4 v[16];
+#pragma unroll
+            for (int j = 0; j < 16; ++j)
+                v[j] = *reinterpret_cast<const uint4*>(in + (16 * p + j) * 128 + ((sx ^ (j & 7)) << 4));
+#pragma unroll
+            for (int w = 0; w < 4; ++w) {
+                // word w of the piece: input columns 16sx + 4w .. +3 = output rows c
+                uint32_t o[4][4];                             // o[i][g]: output row 16sx+4w+i, word g of piece p
+#pragma unroll
+                for (int g = 0; g < 4; ++g) {
+                    const uint32_t a[4] = {(&v[4 * g].x)[w], (&v[4 * g + 1].x)[w], (&v[4 * g + 2].x)[w],
+                                           (&v[4 * g + 3].x)[w]};
+                    uint32_t r[4];
+                    transpose4x4(a, r);
+#pragma unroll
+                    for (int c = 0; c < 4; ++c) o[c][g] = r[c];
+                }
+#pragma unroll
+                for (int c = 0; c < 4; ++c) {
+                    const int row = 16 * sx + 4 * w + c;
+                    *reinterpret_cast<uint4*>(out + row * 128 + ((p ^ (row & 7)) << 4)) =
+                        make_uint4(o[c][0], o[c][1], o[c][2], o[c][3]);
+                }
+            }
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&empty[st]);               // every lane's loads of the stage are consumed
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+            const int64_t t = blockIdx.x + i * gridDim.x;
+            const int64_t nb = t / nkb, kb = t - nb * nkb;
+            tma_store_2d(&tmOut, out, int32_t(nb * 128), int32_t(kb * 128));
+            bulk_commit_group();
+        }
+    }
+    if (!ok && lane == 0) tr_record(FP8_ERR_TIMEOUT);
+    if (lane == 0) bulk_wait_group0();
+    __syncwarp();
+}
+
+// [rows][cols] bytes as 128x128-byte boxes with the 128-byte swizzle.
+inline bool make_tile_map(CUtensorMap* map, const void* base, int64_t rows, int64_t cols) {
+    auto fn = encode_fn();
+    if (!fn) return false;
+    cuuint64_t dims[2] = {cuuint64_t(cols), cuuint64_t(rows)};
+    cuuint64_t strides[1] = {cuuint64_t(cols)};
+    cuuint32_t box[2] = {128u, 128u};
+    cuuint32_t estr[2] = {1u, 1u};
+    return fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2u, const_cast<void*>(base), dims, strides, box, estr,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 }  // namespace fp8bs
@@ -90,10 +194,27 @@ extern "C" int fp8_transpose_128x128(const uint8_t* q, const float* s, int64_t N
                                      fp8_stream_t stream) {
     if (!q || !s || !qT || !sT || N <= 0 || K <= 0) return FP8_ERR_ARG;
     if (N % 128 || K % 128) return FP8_ERR_SHAPE;
+    if (N > (int64_t(1) << 31) - 1 || K > (int64_t(1) << 31) - 1) return FP8_ERR_SHAPE;
     if (!aligned16(q) || !aligned16(qT) || ((reinterpret_cast<uintptr_t>(s) | reinterpret_cast<uintptr_t>(sT)) & 3u))
         return FP8_ERR_ALIGN;
-    const int64_t blocks = (N / 128) * (K / 128);
-    if (blocks > 0x7FFFFFFFll) return FP8_ERR_SHAPE;
-    transpose_128x128_kernel<<<unsigned(blocks), 256, 0, reinterpret_cast<cudaStream_t>(stream)>>>(q, s, N, K, qT, sT);
+    const int sms = device_sms();
+    if (sms <= 0) return FP8_ERR_DEVICE;
+    CUtensorMap mi, mo;
+    if (!make_tile_map(&mi, q, N, K) || !make_tile_map(&mo, qT, K, N)) return FP8_ERR_CUDA;
+    static unsigned char opted[kMaxDevices];
+    if (!opt_in_dynamic_smem(transpose_128x128_kernel, kTrSmem, opted)) return FP8_ERR_CUDA;
+    const int64_t tiles = (N / 128) * (K / 128);
+    const int grid = int(tiles < sms ? tiles : sms);
+    transpose_128x128_kernel<<<grid, kTrThreads, kTrSmem, reinterpret_cast<cudaStream_t>(stream)>>>(
+        mi, mo, s, sT, N / 128, K / 128);
     return cudaGetLastError() == cudaSuccess ? FP8_OK : FP8_ERR_CUDA;
+}
+
+extern "C" int fp8bs_transpose_take_status(cudaStream_t stream) {
+    int v = 0;
+    if (cudaStreamSynchronize(stream) != cudaSuccess) return FP8_ERR_CUDA;
+    if (cudaMemcpyFromSymbol(&v, g_tr_status, sizeof v) != cudaSuccess) return FP8_ERR_CUDA;
+    const int zero = 0;
+    if (cudaMemcpyToSymbol(g_tr_status, &zero, sizeof zero) != cudaSuccess) return FP8_ERR_CUDA;
+    return v;
 }

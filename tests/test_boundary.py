@@ -146,6 +146,7 @@ def test_pow2_and_fused_entry_point_argument_errors(fb):
     assert t(FAKE, FAKE, 100, 128, FAKE, FAKE, None) == -2                                   # N % 128
     assert t(FAKE + 4, FAKE, 128, 128, FAKE, FAKE, None) == -3                               # misaligned q
     assert t(None, FAKE, 128, 128, FAKE, FAKE, None) == -1
+    assert t(FAKE, FAKE, 1 << 31, 128, FAKE, FAKE, None) == -2                              # N past int32 coordinates
     assert "power of two" in fb.fp8_strerror(fb.FP8_ERR_SCALE)
 
 
