@@ -218,13 +218,19 @@ def run_ours(args, ws, rank, local):
     y = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
     flush = L2Flush(dev)
 
+    # The two quantisers are independent HBM-bound passes: W's runs on a side
+    # stream beside X's, and the GEMM waits for both.
+    side = torch.cuda.Stream(dev)
+
     def step(evs=None):
         if evs:
             evs[0].record(stream)
+        side.wait_stream(stream)
+        F.fp8_quant_weight_128x128(w, qw, sw, stream=side)
         F.fp8_quant_act_1x128(x, qx, sx)
         if evs:
             evs[1].record(stream)
-        F.fp8_quant_weight_128x128(w, qw, sw)
+        stream.wait_stream(side)
         if evs:
             evs[2].record(stream)
         F.fp8_gemm_blockscaled(qx, sx, qw, sw, 0, torch.bfloat16, d=y)
@@ -252,8 +258,8 @@ def run_ours(args, ws, rank, local):
     if ws > 1:
         torch.distributed.barrier()
     t_step = [e[0].elapsed_time(e[3]) for e in evs]
-    t_qx = [e[0].elapsed_time(e[1]) for e in evs]
-    t_qw = [e[1].elapsed_time(e[2]) for e in evs]
+    t_qx = [e[0].elapsed_time(e[1]) for e in evs]       # X's quantiser (W's running beside it)
+    t_qw = [e[0].elapsed_time(e[2]) for e in evs]       # both quantisers
     t_gemm = [e[2].elapsed_time(e[3]) for e in evs]
     if F.fp8_get_status() != 0:
         raise RuntimeError("device status set during the timed steps")
@@ -266,7 +272,9 @@ def run_ours(args, ws, rank, local):
     fp8_peak = pk["bf16"] * 2.0             # E4M3 dense = 2x bf16 dense (nominal 4.5 / 2.25 PFLOP/s)
     achieved = GEMM_FLOP / (gemm_ms * 1e-3) / 1e12
 
-    # ---- end to end through the public API from pinned host buffers
+    # ---- end to end through the C-ABI call that takes HOST buffers: X and W
+    # from pinned host memory, Y back to pinned host memory, every copy inside
+    # the events (fp8_linear_host overlaps them with the GPU work by chunks)
     y_h = torch.empty((M, N), dtype=torch.bfloat16).pin_memory()
     e_start, e_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e2e_ms = []
@@ -275,15 +283,14 @@ def run_ours(args, ws, rank, local):
         flush()
         torch.cuda.synchronize()
         e_start.record(stream)
-        x.copy_(x_h, non_blocking=True)
-        w.copy_(w_h, non_blocking=True)
-        step()
-        y_h.copy_(y, non_blocking=True)
+        F.fp8_linear_host(x_h, w_h, y_h)
         e_end.record(stream)
         e_end.synchronize()
         if i >= args.warmup:
             e2e_ms.append(e_start.elapsed_time(e_end))
     e2e = sum(e2e_ms) / len(e2e_ms)
+    if F.fp8_get_status() != 0:
+        raise RuntimeError("device status set during the end-to-end steps")
 
     rows = rows_clocks = None
     if args.rows != "none":
@@ -317,10 +324,12 @@ def run_ours(args, ws, rank, local):
                      "peak_source": "%s bf16 burst x 2 (E4M3/bf16 nominal ratio)" % pk["src"],
                      "frac_of_nominal_4500": round(achieved / FP8_NOMINAL_TFLOPS, 4),
                      "traffic": ncu_traffic()},
-        "step_breakdown_ms": {"quant_act_1x128": round(qx_ms, 5), "quant_weight_128x128": round(qw_ms, 5),
+        "step_breakdown_ms": {"quant_act_1x128_beside_w": round(qx_ms, 5),
+                              "quant_act_and_weight_concurrent": round(qw_ms, 5),
                               "gemm": round(gemm_ms, 5)},
         "e2e": {"value": round(GEMM_FLOP * ws / (e2e * 1e-3) / 1e12, 3), "unit": "TFLOP/s",
                 "ms_per_step": round(e2e, 4), "steps": e2e_steps,
+                "api": "fp8_linear_host: pinned host X, W -> pinned host Y, copies chunked and overlapped",
                 "h2d_bytes_per_step": x.numel() * 2 + w.numel() * 2, "d2h_bytes_per_step": y.numel() * 2},
         # quant_act_1x128, quant_weight_128x128, the GEMM and (when it splits its last wave) its fix-up
         "gpu_launches": (2 + gemm_launches(F, M, N, K, dev)) * args.steps,

@@ -64,6 +64,7 @@ _SIGS = {
     "fp8_moe_combine_bf16": [_P, _I64, _P, _P, _I64, _I, _I64, _P, _P],
     "fp8_get_status": [_P],
     "fp8_selftest_wait_timeout": [ctypes.c_uint64, _P],
+    "fp8_linear_host": [_P, _P, _I64, _I64, _I64, _P, _U32, _P, _I64, _P],
 }
 for _name, _args in _SIGS.items():
     _f = getattr(lib, _name)
@@ -77,6 +78,8 @@ lib.fp8_gemm_split_plan.argtypes = [_I, _I64, _I64, _I64, _I, _I64, _P, _P, _P]
 lib.fp8_gemm_split_plan.restype = _I
 lib.fp8_gemm_split_units.argtypes = [_I, _I64, _I64, _I64, _I, _I64, _I64, _P, _I64]
 lib.fp8_gemm_split_units.restype = _I64
+lib.fp8_linear_host_workspace_bytes.argtypes = [_I64, _I64, _I64]
+lib.fp8_linear_host_workspace_bytes.restype = _I64
 lib.fp8_gemm_tile_cols.argtypes = [_I]
 lib.fp8_gemm_tile_cols.restype = _I
 lib.fp8_strerror.argtypes = [_I]
@@ -87,6 +90,7 @@ lib.fp8_version.restype = _I
 #: every symbol include/fp8bs.h declares
 EXPORTED = sorted(list(_SIGS) + ["fp8_moe_route_workspace_size", "fp8_gemm_blockscaled_workspace_bytes",
                                   "fp8_gemm_split_plan", "fp8_gemm_split_units", "fp8_gemm_tile_cols",
+                                  "fp8_linear_host_workspace_bytes",
                                   "fp8_strerror", "fp8_version"])
 
 
@@ -198,23 +202,40 @@ def _gemm_workspace(device: torch.device, stream_handle: int, M: int, N: int, K:
     return ws, need
 
 
+_LINEAR_WS: dict = {}
+
+
+def _linear_workspace(device: torch.device, stream_handle: int, M: int, N: int, K: int):
+    need = lib.fp8_linear_host_workspace_bytes(M, N, K)
+    if need < 0:
+        _check("fp8_linear_host_workspace_bytes", int(need))
+    key = (device.index, stream_handle)
+    ws = _LINEAR_WS.get(key)
+    if ws is None or ws.numel() < need:
+        ws = torch.empty(need, dtype=torch.uint8, device=device)
+        _LINEAR_WS[key] = ws
+    return ws, need
+
+
 def _workspace_devices() -> list:
-    """The device indices that hold a split workspace (each must be waited
+    """The device indices that hold a cached workspace (each must be waited
     for before its workspace goes back to the caching allocator)."""
-    return sorted({dev for dev, _ in _GEMM_WS})
+    return sorted({dev for dev, _ in _GEMM_WS} | {dev for dev, _ in _LINEAR_WS})
 
 
 def release_gemm_workspaces(_synchronize=torch.cuda.synchronize) -> int:
-    """Free the split workspaces kept per device and stream (one slab per SM
-    pair, 18.9 MB on a 148-SM GPU, per stream that ran a split GEMM).  It
+    """Free the workspaces kept per device and stream: the GEMM split slabs
+    (one per SM pair, 18.9 MB on a 148-SM GPU, per stream that ran a split
+    GEMM) and the device buffers of fp8_linear_host.  It
     first waits for every device that holds one, so no GEMM queued on any
     of them still reads or writes its workspace.  Returns how many were
     freed; later calls allocate again as needed."""
-    n = len(_GEMM_WS)
+    n = len(_GEMM_WS) + len(_LINEAR_WS)
     if n:
         for dev in _workspace_devices():
             _synchronize(dev)
         _GEMM_WS.clear()
+        _LINEAR_WS.clear()
     return n
 
 
@@ -268,6 +289,42 @@ def fp8_gemm_blockscaled(a, sa, b, sb, b_scale_mode: int = FP8_BSCALE_BLOCK128, 
     _check("fp8_gemm_blockscaled_ws", lib.fp8_gemm_blockscaled_ws(
         *args, None if ws is None else ws.data_ptr(), nbytes, st))
     return d
+
+
+def _host_ptr(t: torch.Tensor, name: str) -> int:
+    if t.is_cuda:
+        raise ValueError("%s must be a host (CPU) tensor" % name)
+    if t.dtype != torch.bfloat16:
+        raise TypeError("%s must be torch.bfloat16, got %s" % (name, t.dtype))
+    if not t.is_contiguous():
+        raise ValueError("%s must be contiguous" % name)
+    return t.data_ptr()
+
+
+def fp8_linear_host(x_h: torch.Tensor, w_h: torch.Tensor, y_h: torch.Tensor | None = None, flags: int = 0,
+                    device=None, stream=None) -> torch.Tensor:
+    """Y = X W^T from HOST tensors x_h bf16 [M, K] and w_h bf16 [N, K] into the
+    host tensor y_h bf16 [M, N] (allocated page-locked if not given): the
+    copies in and out, the two quantisations and the GEMM, pipelined over
+    chunks of W on the GPU `device` (default: the current one).  Asynchronous
+    on the stream: y_h holds the result once the stream reaches this call's
+    end (torch.cuda.synchronize, or an event)."""
+    M, K = x_h.shape
+    N = w_h.shape[0]
+    if w_h.shape[1] != K:
+        raise ValueError("x_h and w_h disagree on K")
+    if y_h is None:
+        y_h = torch.empty((M, N), dtype=torch.bfloat16).pin_memory()
+    elif tuple(y_h.shape) != (M, N):
+        raise ValueError("y_h must be [M, N]")
+    dev = torch.device("cuda", torch.cuda.current_device() if device is None else torch.device(device).index)
+    with torch.cuda.device(dev):
+        st = _stream(stream)
+        ws, nbytes = _linear_workspace(dev, st, M, N, K)
+        _check("fp8_linear_host", lib.fp8_linear_host(
+            _host_ptr(x_h, "x_h"), _host_ptr(w_h, "w_h"), M, N, K, _host_ptr(y_h, "y_h"), flags,
+            ws.data_ptr(), nbytes, st))
+    return y_h
 
 
 def fp8_gemm_blockscaled_pow2(a, sa, b, sb, b_scale_mode: int = FP8_BSCALE_BLOCK128, out_dtype=torch.bfloat16,

@@ -229,6 +229,39 @@ FP8_API int fp8_gemm_blockscaled_ws(const uint8_t* a, const float* sa,
                                     void* workspace, int64_t workspace_bytes, fp8_stream_t stream);
 
 /* ------------------------------------------------------------------------
+ * The dense FP8 linear layer called with HOST buffers: Y = X W^T computed as
+ * this library's path (the jp-study.kr page: max-abs 1x128 activation tiles
+ * and 128x128 weight blocks; the tmdrlife.com page: each 128-element K
+ * interval promoted into FP32 with the two scales): fp8_quant_act_1x128 of
+ * X, fp8_quant_weight_128x128 of W, fp8_gemm_blockscaled_ws to bf16.  The
+ * exception to the device-pointer rule above: x_h, w_h and y_h are HOST
+ * pointers.
+ *   x_h  bf16 [M][K] row-major, host memory
+ *   w_h  bf16 [N][K] row-major, host memory
+ *   y_h  bf16 [M][N] row-major, host memory (written)
+ *   flags  0 or FP8_SCALE_POW2 (the quantisers' scale rule)
+ *   workspace  device memory of fp8_linear_host_workspace_bytes(M, N, K)
+ *          bytes, 256-byte aligned, owned by the caller; it holds the device
+ *          copies of X, W and Y, their codes and scales, and the GEMM's split
+ *          workspace, and must not be used by another call until this call's
+ *          work on `stream` ends.
+ * The copies are cut into chunks of W's rows (Y's columns) and run on two
+ * internal streams (created once per device), overlapped with the
+ * quantisation and GEMM of earlier chunks on `stream`; `stream` waits for
+ * all of it, so the call is ordered on `stream` like any other.  Host buffers
+ * in page-locked memory let the copies run asynchronously; pageable ones work
+ * but serialise.  x_h and w_h must not change, and y_h must not be read,
+ * until `stream` reaches the end of the call.
+ * M >= 1, N % 128 == 0, K % 128 == 0.  Errors as the calls it makes;
+ * FP8_ERR_ARG also for a workspace smaller than required, FP8_ERR_ALIGN for
+ * a misaligned one.
+ * ---------------------------------------------------------------------- */
+FP8_API int64_t fp8_linear_host_workspace_bytes(int64_t M, int64_t N, int64_t K);
+FP8_API int fp8_linear_host(const uint16_t* x_h, const uint16_t* w_h, int64_t M, int64_t N, int64_t K,
+                            uint16_t* y_h, uint32_t flags, void* workspace, int64_t workspace_bytes,
+                            fp8_stream_t stream);
+
+/* ------------------------------------------------------------------------
  * The block-scaled GEMM with its result quantised in the epilogue (the tmdrlife.com page:
  * BF16 activations are read from HBM, quantised and written back, only to
  * be read again for the next MMA; quantising the producer's output where it

@@ -147,10 +147,21 @@ def test_pow2_and_fused_entry_point_argument_errors(fb):
     assert t(FAKE + 4, FAKE, 128, 128, FAKE, FAKE, None) == -3                               # misaligned q
     assert t(None, FAKE, 128, 128, FAKE, FAKE, None) == -1
     assert t(FAKE, FAKE, 1 << 31, 128, FAKE, FAKE, None) == -2                              # N past int32 coordinates
+    # dense linear from host buffers: argument checks come before any device access
+    lh = L.fp8_linear_host
+    assert lh(None, FAKE, 128, 128, 128, FAKE, 0, FAKE, 1 << 30, None) == -1                 # null x_h
+    assert lh(FAKE, FAKE, 128, 128, 128, FAKE, 0, None, 1 << 30, None) == -1                 # no workspace
+    assert lh(FAKE, FAKE, 0, 128, 128, FAKE, 0, FAKE, 1 << 30, None) == -1                   # M = 0
+    assert lh(FAKE, FAKE, 128, 128, 128, FAKE, 2, FAKE, 1 << 30, None) == -1                 # unknown flag
+    assert lh(FAKE, FAKE, 128, 100, 128, FAKE, 0, FAKE, 1 << 30, None) == -2                 # N % 128
+    assert lh(FAKE, FAKE, 128, 128, 128, FAKE, 0, FAKE + 16, 1 << 30, None) == -3            # workspace not 256-aligned
+    assert L.fp8_linear_host_workspace_bytes(0, 128, 128) == -1
+    assert L.fp8_linear_host_workspace_bytes(128, 128, 100) == -2
     assert "power of two" in fb.fp8_strerror(fb.FP8_ERR_SCALE)
 
 
 def test_releasing_no_gemm_workspaces_needs_no_gpu(fb):
+    fb.release_gemm_workspaces()          # whatever earlier tests in this process cached
     assert fb.release_gemm_workspaces() == 0
 
 
