@@ -196,6 +196,32 @@ def ncu_traffic():
     return d.get("dram_bytes_per_launch")
 
 
+def link_time(x_h, w_h, y_h, x, w, y, stream, reps=5):
+    """The host link's own time for one step's bytes: X and W host->device
+    beside Y device->host, on two streams, nothing else (best of `reps`).
+    This bounds the end-to-end step: the copies in the two directions share
+    the link, so they take longer together than the one-way copy in."""
+    a, b = torch.cuda.Stream(stream.device), torch.cuda.Stream(stream.device)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    best = float("inf")
+    for _ in range(reps):
+        torch.cuda.synchronize()
+        e0.record(stream)
+        a.wait_stream(stream)
+        b.wait_stream(stream)
+        with torch.cuda.stream(a):
+            x.copy_(x_h, non_blocking=True)
+            w.copy_(w_h, non_blocking=True)
+        with torch.cuda.stream(b):
+            y_h.copy_(y, non_blocking=True)
+        stream.wait_stream(a)
+        stream.wait_stream(b)
+        e1.record(stream)
+        e1.synchronize()
+        best = min(best, e0.elapsed_time(e1))
+    return best
+
+
 # ---------------------------------------------------------------- our arm
 def run_ours(args, ws, rank, local):
     from fp8_fine_grained_16_b300 import build
@@ -251,6 +277,9 @@ def run_ours(args, ws, rank, local):
         torch.distributed.barrier()
     torch.cuda.synchronize()
     with Clocks(local) as clk:
+        # a device-side sleep first, so the host enqueues ahead of the GPU and
+        # no step's events include host launch time
+        torch.cuda._sleep(50_000_000)
         for i in range(args.steps):
             flush()
             step(evs[i])
@@ -291,6 +320,7 @@ def run_ours(args, ws, rank, local):
     e2e = sum(e2e_ms) / len(e2e_ms)
     if F.fp8_get_status() != 0:
         raise RuntimeError("device status set during the end-to-end steps")
+    link = link_time(x_h, w_h, y_h, x, w, y, stream)
 
     rows = rows_clocks = None
     if args.rows != "none":
@@ -330,6 +360,7 @@ def run_ours(args, ws, rank, local):
         "e2e": {"value": round(GEMM_FLOP * ws / (e2e * 1e-3) / 1e12, 3), "unit": "TFLOP/s",
                 "ms_per_step": round(e2e, 4), "steps": e2e_steps,
                 "api": "fp8_linear_host: pinned host X, W -> pinned host Y, copies chunked and overlapped",
+                "link_ms": round(link, 4), "frac_of_link": round(link / e2e, 4),
                 "h2d_bytes_per_step": x.numel() * 2 + w.numel() * 2, "d2h_bytes_per_step": y.numel() * 2},
         # quant_act_1x128, quant_weight_128x128, the GEMM and (when it splits its last wave) its fix-up
         "gpu_launches": (2 + gemm_launches(F, M, N, K, dev)) * args.steps,
@@ -393,27 +424,38 @@ class _SmClock:
 _SM_CLOCK = None
 
 
-def _time(fn, reps, warm, flush, stream):
-    """Median of `reps` event-timed runs, L2 flushed before each; records the
-    median SM clock sampled after each run in _SM_CLOCK.last."""
-    global _SM_CLOCK
-    if _SM_CLOCK is None:
-        _SM_CLOCK = _SmClock()
+def timed_reps(fn, reps, flush, stream):
+    """Device times (ms) of `reps` runs of fn, each timed alone: the GPU is
+    synchronised after every run (so each starts from an idle GPU at its
+    burst clock) and L2 is flushed before it.  Between the flush and the
+    run's first event the device sleeps ~0.2 ms, so the host has enqueued
+    the run before the GPU reaches its events: a run's time never includes
+    the host's time to launch it (which a busy host can stretch past the
+    flush that would otherwise hide it)."""
+    ts = []
     a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    for _ in range(warm):
-        fn()
-    ts, mhz = [], []
     for _ in range(reps):
         flush()
+        torch.cuda._sleep(400_000)
         a.record(stream)
         fn()
         b.record(stream)
         b.synchronize()
         ts.append(a.elapsed_time(b))
-        c = _SM_CLOCK.read()
-        if c is not None:
-            mhz.append(c)
-    _SM_CLOCK.last = statistics.median(mhz) if mhz else _SM_CLOCK.query()
+    return ts
+
+
+def _time(fn, reps, warm, flush, stream):
+    """Median of `reps` event-timed runs, L2 flushed before each; records the
+    SM clock read right after them in _SM_CLOCK.last."""
+    global _SM_CLOCK
+    if _SM_CLOCK is None:
+        _SM_CLOCK = _SmClock()
+    for _ in range(warm):
+        fn()
+    ts = timed_reps(fn, reps, flush, stream)
+    c = _SM_CLOCK.read()
+    _SM_CLOCK.last = c if c is not None else _SM_CLOCK.query()
     return statistics.median(ts)
 
 
@@ -883,17 +925,9 @@ def run_case(name: str, reps: int):
         raise SystemExit("unknown case %r (one of %s)" % (name, ", ".join(CASES)))
     st = torch.cuda.current_stream()
     flush = L2Flush(dev)
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     fn()
     torch.cuda.synchronize()
-    ts = []
-    for _ in range(reps):
-        flush()
-        e0.record(st)
-        fn()
-        e1.record(st)
-        e1.synchronize()
-        ts.append(e0.elapsed_time(e1))
+    ts = timed_reps(fn, reps, flush, st)
     status = F.fp8_get_status()
     print(json.dumps({"case": name, "workload": work, "launches": 1 + reps, "ms_min": round(min(ts), 5),
                       "ms_median": round(statistics.median(ts), 5), "status": status}))

@@ -12,7 +12,9 @@
 // exact in 17 bits and a remainder, e^r by its degree-7 Taylor polynomial in
 // Horner form with fused multiply-adds, one multiply by 2^n), not by the
 // library expf, so h is a fixed function of (g, u) and the codes can be
-// checked bit for bit.  That e^x is within 1 ulp of the exact value.
+// checked bit for bit.  That e^x is within 1 ulp of the exact value.  The
+// reciprocal in sigma is the correctly rounded one, formed by Markstein's
+// correction of the hardware approximation (below).
 //
 // One warp per row; each half-warp quantises 128-column tiles (16 lanes x 8
 // values, 16-byte loads of gate and up; two tiles' loads in flight), the
@@ -59,12 +61,48 @@ FP8_DEV float2 one_plus_exp(float2 x) {
     return __fadd2_rn(make_float2(1.0f, 1.0f), make_float2(x.x > 88.0f ? inf : e.x, x.y > 88.0f ? inf : e.y));
 }
 
+// The correctly rounded reciprocal 1/d of two values d >= 1 (the IEEE
+// quotient), by Markstein's method (P. Markstein, "Computation of elementary
+// functions on the IBM RISC System/6000 processor", IBM J. Res. Dev. 34(1),
+// 1990): from an approximation y within one ulp of 1/d, the residual
+// r = 1 - d*y is exact in one fused multiply-add and y + r*y, rounded once,
+// is the correctly rounded 1/d.  The approximation is the hardware's
+// rcp.approx.ftz.f32 (at most one ulp off).  Reciprocals below the normal
+// range (d >= 2^126), d = +inf and NaN take __frcp_rn instead, which is what
+// every other d matches bit for bit (checked for all d >= 1 by
+// fp8_selftest_reciprocal).
+FP8_DEV float2 rcp_rn_from_one(float2 d) {
+    if (!(d.x < 0x1p126f && d.y < 0x1p126f)) return make_float2(__frcp_rn(d.x), __frcp_rn(d.y));
+    float2 y;
+    asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(y.x) : "f"(d.x));
+    asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(y.y) : "f"(d.y));
+    const float2 r = __ffma2_rn(make_float2(-d.x, -d.y), y, make_float2(1.0f, 1.0f));
+    return __ffma2_rn(r, y, y);
+}
+
 // (g * sigma(g)) * u for two elements, sigma(g) = 1 / (1 + e^-g); the
 // reciprocal is the correctly rounded one, equal to the IEEE quotient.
 FP8_DEV float2 swiglu2_fp32(float2 g, float2 u) {
     const float2 d = one_plus_exp(make_float2(-g.x, -g.y));
-    const float2 sig = make_float2(__frcp_rn(d.x), __frcp_rn(d.y));
+    const float2 sig = rcp_rn_from_one(d);
     return __fmul2_rn(__fmul2_rn(g, sig), u);
+}
+
+// Every float d with bits in [lo, hi] (d >= 1): rcp_rn_from_one(d) against
+// __frcp_rn(d), bit for bit; the count of differences is added to *bad.
+__global__ void __launch_bounds__(256) reciprocal_selftest_kernel(uint32_t lo, uint32_t hi,
+                                                                  unsigned long long* bad) {
+    const uint64_t stride = uint64_t(gridDim.x) * blockDim.x * 2;
+    unsigned long long n = 0;
+    for (uint64_t b = uint64_t(lo) + (uint64_t(blockIdx.x) * blockDim.x + threadIdx.x) * 2; b <= hi; b += stride) {
+        const bool two = b + 1 <= hi;
+        const float2 d = make_float2(__uint_as_float(uint32_t(b)), __uint_as_float(uint32_t(two ? b + 1 : b)));
+        const float2 r = rcp_rn_from_one(d);
+        n += __float_as_uint(r.x) != __float_as_uint(__frcp_rn(d.x));
+        if (two) n += __float_as_uint(r.y) != __float_as_uint(__frcp_rn(d.y));
+    }
+    for (int o = 16; o > 0; o >>= 1) n += __shfl_xor_sync(0xFFFFFFFFu, n, o);
+    if ((threadIdx.x & 31) == 0 && n) atomicAdd(bad, n);
 }
 
 constexpr int kSgRows = 8;          // rows (warps) per CTA
@@ -131,6 +169,18 @@ __global__ void __launch_bounds__(256) swiglu_quant_1x128_kernel(const uint16_t*
 }  // namespace fp8bs
 
 using namespace fp8bs;
+
+extern "C" int fp8_selftest_reciprocal(uint32_t first_bits, uint32_t last_bits, unsigned long long* mismatches,
+                                       fp8_stream_t stream) {
+    if (!mismatches || first_bits < 0x3F800000u || last_bits < first_bits) return FP8_ERR_ARG;
+    if (reinterpret_cast<uintptr_t>(mismatches) & 7u) return FP8_ERR_ALIGN;
+    const uint64_t n = uint64_t(last_bits) - first_bits + 1;
+    const uint64_t blocks = (n / 2 + 255) / 256;
+    const unsigned grid = unsigned(blocks < 148 * 16 ? (blocks ? blocks : 1) : 148 * 16);
+    reciprocal_selftest_kernel<<<grid, 256, 0, reinterpret_cast<cudaStream_t>(stream)>>>(first_bits, last_bits,
+                                                                                          mismatches);
+    return cudaGetLastError() == cudaSuccess ? FP8_OK : FP8_ERR_CUDA;
+}
 
 extern "C" int fp8_swiglu_quant_1x128(const uint16_t* y, int64_t R, int64_t I, int64_t ldy, uint8_t* q, float* s,
                                       uint32_t flags, fp8_stream_t stream) {

@@ -64,6 +64,7 @@ _SIGS = {
     "fp8_moe_combine_bf16": [_P, _I64, _P, _P, _I64, _I, _I64, _P, _P],
     "fp8_get_status": [_P],
     "fp8_selftest_wait_timeout": [ctypes.c_uint64, _P],
+    "fp8_selftest_reciprocal": [_U32, _U32, _P, _P],
     "fp8_linear_host": [_P, _P, _I64, _I64, _I64, _P, _U32, _P, _I64, _P],
 }
 for _name, _args in _SIGS.items():
@@ -485,6 +486,18 @@ def fp8_moe_combine_bf16(y, pos, gate, out=None, stream=None) -> torch.Tensor:
         _ptr(y, torch.bfloat16, "y"), rows, _ptr(pos, torch.int32, "pos"), _ptr(gate, torch.float32, "gate"), T, k, N,
         _ptr(out, torch.bfloat16, "out"), _stream(stream)))
     return out
+
+
+def fp8_selftest_reciprocal(first_bits: int = 0x3F800000, last_bits: int = 0x7FFFFFFF, device=None) -> int:
+    """How many floats d >= 1 with bits in [first_bits, last_bits] get a
+    reciprocal in the SwiGLU kernel that differs from __frcp_rn (synchronises)."""
+    dev = torch.device("cuda", torch.cuda.current_device() if device is None else torch.device(device).index)
+    bad = torch.zeros(1, dtype=torch.int64, device=dev)
+    with torch.cuda.device(dev):
+        _check("fp8_selftest_reciprocal", lib.fp8_selftest_reciprocal(first_bits, last_bits, bad.data_ptr(),
+                                                                      _stream(None)))
+        torch.cuda.synchronize(dev)
+    return int(bad.item())
 
 
 def fp8_get_status(stream=None) -> int:

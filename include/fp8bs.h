@@ -454,6 +454,18 @@ FP8_API int fp8_get_status(fp8_stream_t stream);
  * ---------------------------------------------------------------------- */
 FP8_API int fp8_selftest_wait_timeout(uint64_t timeout_ns, fp8_stream_t stream);
 
+/* ------------------------------------------------------------------------
+ * Reciprocal self-test (no counterpart on the pages): the SwiGLU kernel's
+ * sigma = 1/d (d = 1 + e^-g >= 1) comes from the hardware approximation
+ * corrected by Markstein's method; this counts, for every float d whose bit
+ * pattern lies in [first_bits, last_bits], the d where that reciprocal
+ * differs in any bit from __frcp_rn(d), adding the count to *mismatches
+ * (a device counter the caller zeroes).  first_bits >= 0x3F800000 (d >= 1);
+ * [0x3F800000, 0x7FFFFFFF] covers every d >= 1, +inf and the NaNs.
+ * ---------------------------------------------------------------------- */
+FP8_API int fp8_selftest_reciprocal(uint32_t first_bits, uint32_t last_bits, unsigned long long* mismatches,
+                                    fp8_stream_t stream);
+
 /* Human-readable name of a status code (static string). */
 FP8_API const char* fp8_strerror(int code);
 

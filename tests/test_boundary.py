@@ -147,6 +147,11 @@ def test_pow2_and_fused_entry_point_argument_errors(fb):
     assert t(FAKE + 4, FAKE, 128, 128, FAKE, FAKE, None) == -3                               # misaligned q
     assert t(None, FAKE, 128, 128, FAKE, FAKE, None) == -1
     assert t(FAKE, FAKE, 1 << 31, 128, FAKE, FAKE, None) == -2                              # N past int32 coordinates
+    # reciprocal self-test: d >= 1 only, and an aligned counter
+    rs = L.fp8_selftest_reciprocal
+    assert rs(0x3F7FFFFF, 0x3F800000, FAKE, None) == -1                                       # d < 1
+    assert rs(0x3F800001, 0x3F800000, FAKE, None) == -1                                       # empty range
+    assert rs(0x3F800000, 0x3F800001, FAKE + 4, None) == -3                                   # misaligned counter
     # dense linear from host buffers: argument checks come before any device access
     lh = L.fp8_linear_host
     assert lh(None, FAKE, 128, 128, 128, FAKE, 0, FAKE, 1 << 30, None) == -1                 # null x_h

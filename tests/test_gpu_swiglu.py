@@ -113,3 +113,10 @@ def test_swiglu_quant_extremes_against_fp64_definition(fb, orc):
         assert n_mid <= 2
         if flags & 1:
             assert n_scale <= 1
+
+
+def test_reciprocal_matches_frcp_rn_for_every_d_from_one(fb):
+    """The kernel's sigma = 1/d (Markstein's correction of the hardware
+    approximation) equals __frcp_rn bit for bit for every float d >= 1, +inf
+    and every NaN pattern: all 2^30 + 2^23 bit patterns from 0x3F800000."""
+    assert fb.fp8_selftest_reciprocal(0x3F800000, 0x7FFFFFFF) == 0
