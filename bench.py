@@ -820,7 +820,7 @@ def run_reference(args, ws, rank):
 
 # ---------------------------------------------------------------- single-kernel cases (for ncu)
 CASES = ("dense", "wgrad", "wgrad_small", "q8", "dgrad_transpose", "quant_1x128", "quant_128x1", "quant_128x128",
-         "grouped_up_small", "grouped_down_small", "permute", "combine", "swiglu", "pow2_dense")
+         "grouped_up_small", "grouped_down_small", "route", "permute", "combine", "swiglu", "pow2_dense")
 
 
 def run_case(name: str, reps: int):
@@ -903,6 +903,12 @@ def run_case(name: str, reps: int):
         y = torch.empty((R, Ng), dtype=torch.bfloat16, device=dev)
         fn = lambda: F.fp8_grouped_gemm_blockscaled(a, sa, b, sb, off, d=y)
         work = "%d rows, 32 experts, N=%d, K=%d" % (R, Ng, Kg)
+    elif name == "route":
+        logits = torch.randn((4096, 256), device=dev, generator=g)
+        r = F.fp8_moe_route_topk(logits, 8)
+        wk = torch.empty(max(1, F.fp8_moe_route_workspace_size(4096, 256) // 4), dtype=torch.int32, device=dev)
+        fn = lambda: F.fp8_moe_route_topk(logits, 8, out=r, work=wk)
+        work = "logits [4096,256] -> top-8, offsets, positions"
     elif name in ("permute", "combine"):
         logits = torch.randn((4096, 256), device=dev, generator=g)
         r = F.fp8_moe_route_topk(logits, 8)

@@ -28,28 +28,40 @@ constexpr int kMaxE = 1024;
 constexpr int kMaxK = 32;
 
 // ------------------------------------------------------------------ routing, kernel 1
-// 256 threads = 8 warps; each warp routes 8 tokens of the chunk.  Lane l
-// holds logits e = l + 32j (j < EPL).  Each of the k rounds takes the
-// warp-wide maximum among unselected experts, the lower index winning ties.
+// 1024 threads = 32 warps per chunk; warp w routes tokens w and w + 32 of
+// the chunk, loading both tokens' logits before either is ranked so that
+// their loads are in flight together.  Lane l holds logits e = l + 32j
+// (j < EPL).  Each of the k rounds takes the warp-wide maximum among
+// unselected experts, the lower index winning ties.
+constexpr int kTopkWarps = 32;
+constexpr int kTokensPerWarp = kChunk / kTopkWarps;
+
 template <int EPL>
-__global__ void __launch_bounds__(256) route_topk_kernel(const float* __restrict__ logits, int64_t T, int E, int k,
-                                                        int32_t* __restrict__ idx, float* __restrict__ gate,
-                                                        int32_t* __restrict__ work) {
+__global__ void __launch_bounds__(32 * kTopkWarps) route_topk_kernel(const float* __restrict__ logits, int64_t T,
+                                                                     int E, int k, int32_t* __restrict__ idx,
+                                                                     float* __restrict__ gate,
+                                                                     int32_t* __restrict__ work) {
     __shared__ int cnt[kMaxE];
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     for (int e = threadIdx.x; e < E; e += blockDim.x) cnt[e] = 0;
     __syncthreads();
 
     const int64_t t0 = int64_t(blockIdx.x) * kChunk;
-    for (int tt = warp; tt < kChunk; tt += 8) {
-        const int64_t t = t0 + tt;
-        if (t >= T) break;
-        float v[EPL];
+    float vv[kTokensPerWarp][EPL];
+#pragma unroll
+    for (int u = 0; u < kTokensPerWarp; ++u) {
+        const int64_t t = t0 + warp + kTopkWarps * u;
 #pragma unroll
         for (int j = 0; j < EPL; ++j) {
             const int e = lane + 32 * j;
-            v[j] = e < E ? __ldg(logits + t * E + e) : 0.0f;
+            vv[u][j] = (t < T && e < E) ? __ldg(logits + t * E + e) : 0.0f;
         }
+    }
+#pragma unroll
+    for (int u = 0; u < kTokensPerWarp; ++u) {
+        const int64_t t = t0 + warp + kTopkWarps * u;
+        if (t >= T) break;
+        const float (&v)[EPL] = vv[u];
         uint32_t taken = 0;                          // bit j: expert lane+32j already selected
         int my_e = -1;                               // lane j < k keeps slot j
         float my_v = 0.0f;
@@ -96,26 +108,36 @@ __global__ void __launch_bounds__(256) route_topk_kernel(const float* __restrict
 
 // ------------------------------------------------------------------ routing, kernel 2
 // work[c][e] (pairs of chunk c that chose expert e) -> the running total over
-// chunks 0..c, in place.  One thread per expert walks the chunks; the loads
-// of a warp are one 128-byte row segment, eight chunks in flight.
+// chunks 0..c, in place.  One warp per expert: lane l takes chunk c0 + l of
+// each group of 32 chunks, a shuffle scan forms the group's running totals,
+// and the group's sum carries into the next group.  Four groups' loads are
+// issued before any of them is scanned.
+constexpr int kScanGroups = 4;
+
 __global__ void __launch_bounds__(256) route_chunk_scan_kernel(int32_t* __restrict__ work, int64_t nchunks, int E) {
-    const int e = blockIdx.x * blockDim.x + threadIdx.x;
-    if (e >= E) return;
-    int run = 0;
-    int64_t c = 0;
-    for (; c + 8 <= nchunks; c += 8) {
-        int v[8];
+    const int lane = threadIdx.x & 31;
+    const int e = blockIdx.x * 8 + (threadIdx.x >> 5);
+    if (e >= E) return;                                       // warp-uniform
+    int carry = 0;
+    for (int64_t c0 = 0; c0 < nchunks; c0 += 32 * kScanGroups) {
+        int v[kScanGroups];
 #pragma unroll
-        for (int i = 0; i < 8; ++i) v[i] = work[(c + i) * E + e];
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-            run += v[i];
-            work[(c + i) * E + e] = run;
+        for (int g = 0; g < kScanGroups; ++g) {
+            const int64_t c = c0 + 32 * g + lane;
+            v[g] = c < nchunks ? work[c * E + e] : 0;
         }
-    }
-    for (; c < nchunks; ++c) {
-        run += work[c * E + e];
-        work[c * E + e] = run;
+#pragma unroll
+        for (int g = 0; g < kScanGroups; ++g) {
+            int x = v[g];
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const int y = __shfl_up_sync(0xFFFFFFFFu, x, o);
+                if (lane >= o) x += y;
+            }
+            const int64_t c = c0 + 32 * g + lane;
+            if (c < nchunks) work[c * E + e] = carry + x;
+            carry += __shfl_sync(0xFFFFFFFFu, x, 31);
+        }
     }
 }
 
@@ -332,14 +354,15 @@ extern "C" int fp8_moe_route_topk(const float* logits, int64_t T, int E, int top
     if (nchunks > 0x7FFFFFFFll) return FP8_ERR_SHAPE;
     const int epl = (E + 31) / 32;
     const unsigned g = unsigned(nchunks);
-    if (epl <= 1) route_topk_kernel<1><<<g, 256, 0, s>>>(logits, T, E, topk, idx, gate, work);
-    else if (epl <= 2) route_topk_kernel<2><<<g, 256, 0, s>>>(logits, T, E, topk, idx, gate, work);
-    else if (epl <= 4) route_topk_kernel<4><<<g, 256, 0, s>>>(logits, T, E, topk, idx, gate, work);
-    else if (epl <= 8) route_topk_kernel<8><<<g, 256, 0, s>>>(logits, T, E, topk, idx, gate, work);
-    else if (epl <= 16) route_topk_kernel<16><<<g, 256, 0, s>>>(logits, T, E, topk, idx, gate, work);
-    else route_topk_kernel<32><<<g, 256, 0, s>>>(logits, T, E, topk, idx, gate, work);
+    constexpr unsigned kTb = 32 * kTopkWarps;
+    if (epl <= 1) route_topk_kernel<1><<<g, kTb, 0, s>>>(logits, T, E, topk, idx, gate, work);
+    else if (epl <= 2) route_topk_kernel<2><<<g, kTb, 0, s>>>(logits, T, E, topk, idx, gate, work);
+    else if (epl <= 4) route_topk_kernel<4><<<g, kTb, 0, s>>>(logits, T, E, topk, idx, gate, work);
+    else if (epl <= 8) route_topk_kernel<8><<<g, kTb, 0, s>>>(logits, T, E, topk, idx, gate, work);
+    else if (epl <= 16) route_topk_kernel<16><<<g, kTb, 0, s>>>(logits, T, E, topk, idx, gate, work);
+    else route_topk_kernel<32><<<g, kTb, 0, s>>>(logits, T, E, topk, idx, gate, work);
     if (cudaGetLastError() != cudaSuccess) return FP8_ERR_CUDA;
-    route_chunk_scan_kernel<<<unsigned((E + 255) / 256), 256, 0, s>>>(work, nchunks, E);
+    route_chunk_scan_kernel<<<unsigned((E + 7) / 8), 256, 0, s>>>(work, nchunks, E);
     if (cudaGetLastError() != cudaSuccess) return FP8_ERR_CUDA;
     route_positions_kernel<<<g, 512, 0, s>>>(idx, T, E, topk, work, nchunks, expert_offsets, src_row, pos);
     return cudaGetLastError() == cudaSuccess ? FP8_OK : FP8_ERR_CUDA;
