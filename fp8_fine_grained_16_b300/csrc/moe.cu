@@ -28,82 +28,66 @@ constexpr int kMaxE = 1024;
 constexpr int kMaxK = 32;
 
 // ------------------------------------------------------------------ routing, kernel 1
-// 1024 threads = 32 warps per chunk; warp w routes tokens w and w + 32 of
-// the chunk, loading both tokens' logits before either is ranked so that
-// their loads are in flight together.  Lane l holds logits e = l + 32j
-// (j < EPL).  Each of the k rounds takes the warp-wide maximum among
-// unselected experts, the lower index winning ties.
-constexpr int kTopkWarps = 32;
-constexpr int kTokensPerWarp = kChunk / kTopkWarps;
-
+// One warp per token, 8 tokens per CTA (so every SM takes part: the ranking
+// is ALU-bound).  Lane l holds logits e = l + 32j (j < EPL).  Each of the k
+// rounds takes the warp-wide maximum among unselected experts, the lower
+// index winning ties.  Each selected (token, expert) pair is counted into
+// work[chunk][expert] (chunk = token / 64) with a global atomic; the caller
+// zeroes work first.
 template <int EPL>
-__global__ void __launch_bounds__(32 * kTopkWarps) route_topk_kernel(const float* __restrict__ logits, int64_t T,
-                                                                     int E, int k, int32_t* __restrict__ idx,
-                                                                     float* __restrict__ gate,
-                                                                     int32_t* __restrict__ work) {
-    __shared__ int cnt[kMaxE];
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    for (int e = threadIdx.x; e < E; e += blockDim.x) cnt[e] = 0;
-    __syncthreads();
-
-    const int64_t t0 = int64_t(blockIdx.x) * kChunk;
-    float vv[kTokensPerWarp][EPL];
+__global__ void __launch_bounds__(256) route_topk_kernel(const float* __restrict__ logits, int64_t T, int E, int k,
+                                                        int32_t* __restrict__ idx, float* __restrict__ gate,
+                                                        int32_t* __restrict__ work) {
+    const int lane = threadIdx.x & 31;
+    const int64_t t = int64_t(blockIdx.x) * 8 + (threadIdx.x >> 5);
+    pdl_launch_dependents();
+    if (t >= T) return;                                   // warp-uniform
+    float v[EPL];
 #pragma unroll
-    for (int u = 0; u < kTokensPerWarp; ++u) {
-        const int64_t t = t0 + warp + kTopkWarps * u;
+    for (int j = 0; j < EPL; ++j) {
+        const int e = lane + 32 * j;
+        v[j] = e < E ? __ldg(logits + t * E + e) : 0.0f;
+    }
+    uint32_t taken = 0;                          // bit j: expert lane+32j already selected
+    int my_e = -1;                               // lane j < k keeps slot j
+    float my_v = 0.0f;
+    for (int r = 0; r < k; ++r) {
+        float bv = 0.0f;
+        int be = 0x7FFFFFFF;
 #pragma unroll
         for (int j = 0; j < EPL; ++j) {
             const int e = lane + 32 * j;
-            vv[u][j] = (t < T && e < E) ? __ldg(logits + t * E + e) : 0.0f;
+            if (e < E && !((taken >> j) & 1u) && (be == 0x7FFFFFFF || v[j] > bv)) {
+                bv = v[j];
+                be = e;
+            }
+        }
+#pragma unroll
+        for (int o = 16; o >= 1; o >>= 1) {
+            const float ov = __shfl_xor_sync(0xFFFFFFFFu, bv, o);
+            const int oe = __shfl_xor_sync(0xFFFFFFFFu, be, o);
+            if (oe != 0x7FFFFFFF && (be == 0x7FFFFFFF || ov > bv || (ov == bv && oe < be))) {
+                bv = ov;
+                be = oe;
+            }
+        }
+        if ((be & 31) == lane) taken |= 1u << (be >> 5);
+        if (lane == r) {
+            my_e = be;
+            my_v = bv;
         }
     }
+    const float vmax = __shfl_sync(0xFFFFFFFFu, my_v, 0);
+    const float ex = lane < k ? expf(my_v - vmax) : 0.0f;
+    float z = ex;
 #pragma unroll
-    for (int u = 0; u < kTokensPerWarp; ++u) {
-        const int64_t t = t0 + warp + kTopkWarps * u;
-        if (t >= T) break;
-        const float (&v)[EPL] = vv[u];
-        uint32_t taken = 0;                          // bit j: expert lane+32j already selected
-        int my_e = -1;                               // lane j < k keeps slot j
-        float my_v = 0.0f;
-        for (int r = 0; r < k; ++r) {
-            float bv = 0.0f;
-            int be = 0x7FFFFFFF;
-#pragma unroll
-            for (int j = 0; j < EPL; ++j) {
-                const int e = lane + 32 * j;
-                if (e < E && !((taken >> j) & 1u) && (be == 0x7FFFFFFF || v[j] > bv)) {
-                    bv = v[j];
-                    be = e;
-                }
-            }
-#pragma unroll
-            for (int o = 16; o >= 1; o >>= 1) {
-                const float ov = __shfl_xor_sync(0xFFFFFFFFu, bv, o);
-                const int oe = __shfl_xor_sync(0xFFFFFFFFu, be, o);
-                if (oe != 0x7FFFFFFF && (be == 0x7FFFFFFF || ov > bv || (ov == bv && oe < be))) {
-                    bv = ov;
-                    be = oe;
-                }
-            }
-            if ((be & 31) == lane) taken |= 1u << (be >> 5);
-            if (lane == r) {
-                my_e = be;
-                my_v = bv;
-            }
-        }
-        const float vmax = __shfl_sync(0xFFFFFFFFu, my_v, 0);
-        const float ex = lane < k ? expf(my_v - vmax) : 0.0f;
-        float z = ex;
-#pragma unroll
-        for (int o = 16; o >= 1; o >>= 1) z += __shfl_xor_sync(0xFFFFFFFFu, z, o);
-        if (lane < k) {
-            idx[t * k + lane] = my_e;
-            gate[t * k + lane] = __fdiv_rn(ex, z);
-            atomicAdd(&cnt[my_e], 1);
-        }
+    for (int o = 16; o >= 1; o >>= 1) z += __shfl_xor_sync(0xFFFFFFFFu, z, o);
+    pdl_wait();                                           // work has been zeroed
+    if (lane < k) {
+        idx[t * k + lane] = my_e;
+        gate[t * k + lane] = __fdiv_rn(ex, z);
+        atomicAdd(&work[(t / kChunk) * E + my_e], 1);
     }
-    __syncthreads();
-    for (int e = threadIdx.x; e < E; e += blockDim.x) work[int64_t(blockIdx.x) * E + e] = cnt[e];
 }
 
 // ------------------------------------------------------------------ routing, kernel 2
@@ -117,6 +101,8 @@ constexpr int kScanGroups = 4;
 __global__ void __launch_bounds__(256) route_chunk_scan_kernel(int32_t* __restrict__ work, int64_t nchunks, int E) {
     const int lane = threadIdx.x & 31;
     const int e = blockIdx.x * 8 + (threadIdx.x >> 5);
+    pdl_launch_dependents();
+    pdl_wait();                                               // the counts are complete
     if (e >= E) return;                                       // warp-uniform
     int carry = 0;
     for (int64_t c0 = 0; c0 < nchunks; c0 += 32 * kScanGroups) {
@@ -158,6 +144,7 @@ __global__ void __launch_bounds__(512) route_positions_kernel(const int32_t* __r
     __shared__ int warp_sum[16];
     const int tid = threadIdx.x;
     const int64_t chunk = blockIdx.x;
+    pdl_wait();                                               // idx and the running totals are complete
 
     for (int e = tid; e < E; e += blockDim.x) {
         scan[e] = __ldg(work + (nchunks - 1) * E + e);
@@ -354,17 +341,24 @@ extern "C" int fp8_moe_route_topk(const float* logits, int64_t T, int E, int top
     if (nchunks > 0x7FFFFFFFll) return FP8_ERR_SHAPE;
     const int epl = (E + 31) / 32;
     const unsigned g = unsigned(nchunks);
-    constexpr unsigned kTb = 32 * kTopkWarps;
-    if (epl <= 1) route_topk_kernel<1><<<g, kTb, 0, s>>>(logits, T, E, topk, idx, gate, work);
-    else if (epl <= 2) route_topk_kernel<2><<<g, kTb, 0, s>>>(logits, T, E, topk, idx, gate, work);
-    else if (epl <= 4) route_topk_kernel<4><<<g, kTb, 0, s>>>(logits, T, E, topk, idx, gate, work);
-    else if (epl <= 8) route_topk_kernel<8><<<g, kTb, 0, s>>>(logits, T, E, topk, idx, gate, work);
-    else if (epl <= 16) route_topk_kernel<16><<<g, kTb, 0, s>>>(logits, T, E, topk, idx, gate, work);
-    else route_topk_kernel<32><<<g, kTb, 0, s>>>(logits, T, E, topk, idx, gate, work);
+    if (cudaMemsetAsync(work, 0, size_t(nchunks) * size_t(E) * sizeof(int32_t), s) != cudaSuccess) return FP8_ERR_CUDA;
+    const unsigned gt = unsigned((T + 7) / 8);
+    if (epl <= 1) route_topk_kernel<1><<<gt, 256, 0, s>>>(logits, T, E, topk, idx, gate, work);
+    else if (epl <= 2) route_topk_kernel<2><<<gt, 256, 0, s>>>(logits, T, E, topk, idx, gate, work);
+    else if (epl <= 4) route_topk_kernel<4><<<gt, 256, 0, s>>>(logits, T, E, topk, idx, gate, work);
+    else if (epl <= 8) route_topk_kernel<8><<<gt, 256, 0, s>>>(logits, T, E, topk, idx, gate, work);
+    else if (epl <= 16) route_topk_kernel<16><<<gt, 256, 0, s>>>(logits, T, E, topk, idx, gate, work);
+    else route_topk_kernel<32><<<gt, 256, 0, s>>>(logits, T, E, topk, idx, gate, work);
     if (cudaGetLastError() != cudaSuccess) return FP8_ERR_CUDA;
-    route_chunk_scan_kernel<<<unsigned((E + 7) / 8), 256, 0, s>>>(work, nchunks, E);
+    // the scan and the positions start early (programmatic dependent
+    // launches) and wait inside for the kernel before them
+    if (launch_pdl(route_chunk_scan_kernel, dim3(unsigned((E + 7) / 8)), dim3(256), 0, s, work, nchunks, E) !=
+        cudaSuccess)
+        return FP8_ERR_CUDA;
     if (cudaGetLastError() != cudaSuccess) return FP8_ERR_CUDA;
-    route_positions_kernel<<<g, 512, 0, s>>>(idx, T, E, topk, work, nchunks, expert_offsets, src_row, pos);
+    if (launch_pdl(route_positions_kernel, dim3(g), dim3(512), 0, s, static_cast<const int32_t*>(idx), T, E, topk,
+                   static_cast<const int32_t*>(work), nchunks, expert_offsets, src_row, pos) != cudaSuccess)
+        return FP8_ERR_CUDA;
     return cudaGetLastError() == cudaSuccess ? FP8_OK : FP8_ERR_CUDA;
 }
 
