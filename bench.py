@@ -819,7 +819,8 @@ def run_reference(args, ws, rank):
 
 
 # ---------------------------------------------------------------- single-kernel cases (for ncu)
-CASES = ("dense", "wgrad", "wgrad_small", "q8", "dgrad_transpose", "quant_1x128", "quant_128x1", "quant_128x128",
+CASES = ("dense", "wgrad", "wgrad_small", "q8", "dgrad_transpose", "quant_1x128", "quant_1x128_h", "quant_128x1",
+         "quant_128x128",
          "grouped_up_small", "grouped_down_small", "route", "permute", "combine", "swiglu", "pow2_dense")
 
 
@@ -884,6 +885,11 @@ def run_case(name: str, reps: int):
         qx, sx = F.fp8_quant_act_1x128(x)
         fn = lambda: F.fp8_quant_act_1x128(x, qx, sx)
         work = "X [4096,7168]"
+    elif name == "quant_1x128_h":
+        x = bf16(32768, 2048)
+        qx, sx = F.fp8_quant_act_1x128(x)
+        fn = lambda: F.fp8_quant_act_1x128(x, qx, sx)
+        work = "h [32768,2048]"
     elif name == "quant_128x1":
         x = bf16(8192, 7168)
         qT, sT = F.fp8_quant_act_128x1(x)
