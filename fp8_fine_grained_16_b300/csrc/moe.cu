@@ -6,11 +6,13 @@
 //             softmax gates over the selected logits, and a stable
 //             counting sort of (token, slot) pairs by expert:
 //               kernel 1: one warp per token -> idx, gate, per-chunk counts
-//               kernel 2: one thread per expert turns the counts into
+//                         (global atomics into a zeroed workspace)
+//               kernel 2: one warp per expert turns the counts into
 //                         running totals over the chunks, in place
 //               kernel 3: per chunk of 64 tokens -> expert offsets and the
 //                         rank of each pair among the chunk's pairs of the
 //                         same expert (64-bit token masks + popcount)
+//             kernels 2 and 3 are programmatic dependent launches.
 //   permute   gathers FP8 rows and their K-block scales (dispatch)
 //   combine   out[t] = sum_j gate[t][j] * y[pos[t][j]] in fp32 -> bf16
 #include <mutex>
