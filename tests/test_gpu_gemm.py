@@ -205,7 +205,7 @@ def test_tensor_core_accumulation_precision_probe(fb, orc):
 @pytest.mark.parametrize("N,K", [(128, 128), (256, 384), (896, 512), (1152, 7040), (7168, 7168)])
 def test_transpose_128x128_bit_exact(fb, N, K):
     """One block, fewer blocks than SMs, several blocks per CTA with a ragged
-    last round (1152 x 7040: 495 blocks), and the full weight (3136 blocks)."""
+    last pass over the CTAs (1152 x 7040: 495 blocks), and the full weight (3136 blocks)."""
     q = rand_codes((N, K), N + K)
     s = rand_scales((N // 128, K // 128), N)
     qT, sT = fb.fp8_transpose_128x128(_dev(q), _dev(s))
