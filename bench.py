@@ -821,7 +821,8 @@ def run_reference(args, ws, rank):
 # ---------------------------------------------------------------- single-kernel cases (for ncu)
 CASES = ("dense", "wgrad", "wgrad_small", "q8", "dgrad_transpose", "quant_1x128", "quant_1x128_h", "quant_128x1",
          "quant_128x128",
-         "grouped_up_small", "grouped_down_small", "route", "permute", "combine", "swiglu", "pow2_dense")
+         "grouped_up_small", "grouped_down_small", "grouped_down_small_pow2", "route", "permute", "combine", "swiglu",
+         "pow2_dense", "pow2_wgrad_small")
 
 
 def run_case(name: str, reps: int):
@@ -868,12 +869,16 @@ def run_case(name: str, reps: int):
             y = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
             fn = lambda: F.fp8_gemm_blockscaled(a, sa, b, sb, 0, torch.bfloat16, d=y)
         work = "%dx%dx%d" % (M, N, K)
-    elif name in ("wgrad", "wgrad_small"):
+    elif name in ("wgrad", "wgrad_small", "pow2_wgrad_small"):
         H, T = (7168, 8192) if name == "wgrad" else (2048, 8192)
         a, b = codes(H, T), codes(H, T)
         sa, sb = scales(T // 128, H), scales(T // 128, H)
         dw = torch.empty((H, H), dtype=torch.float32, device=dev)
-        fn = lambda: F.fp8_gemm_blockscaled(a, sa, b, sb, F.FP8_BSCALE_ROW, torch.float32, d=dw)
+        if name == "pow2_wgrad_small":
+            sa, sb = torch.exp2(torch.round(torch.log2(sa))), torch.exp2(torch.round(torch.log2(sb)))
+            fn = lambda: F.fp8_gemm_blockscaled_pow2(a, sa, b, sb, F.FP8_BSCALE_ROW, torch.float32, d=dw)
+        else:
+            fn = lambda: F.fp8_gemm_blockscaled(a, sa, b, sb, F.FP8_BSCALE_ROW, torch.float32, d=dw)
         work = "%dx%dx%d, per-row B scales, fp32 out" % (H, H, T)
     elif name == "dgrad_transpose":
         q, sq = codes(N, K), scales(N // 128, K // 128)
@@ -900,14 +905,18 @@ def run_case(name: str, reps: int):
         qw, sw = F.fp8_quant_weight_128x128(w)
         fn = lambda: F.fp8_quant_weight_128x128(w, qw, sw)
         work = "W [7168,7168]"
-    elif name in ("grouped_up_small", "grouped_down_small"):
+    elif name in ("grouped_up_small", "grouped_down_small", "grouped_down_small_pow2"):
         E = 32
         Ng, Kg = (4096, 7168) if name == "grouped_up_small" else (7168, 2048)
         off, R = offsets(E)
         a, sa = codes(R, Kg), scales(Kg // 128, R)
         b, sb = codes(E, Ng, Kg), scales(E, Ng // 128, Kg // 128)
         y = torch.empty((R, Ng), dtype=torch.bfloat16, device=dev)
-        fn = lambda: F.fp8_grouped_gemm_blockscaled(a, sa, b, sb, off, d=y)
+        if name == "grouped_down_small_pow2":
+            sa, sb = torch.exp2(torch.round(torch.log2(sa))), torch.exp2(torch.round(torch.log2(sb)))
+            fn = lambda: F.fp8_grouped_gemm_blockscaled_pow2(a, sa, b, sb, off, d=y)
+        else:
+            fn = lambda: F.fp8_grouped_gemm_blockscaled(a, sa, b, sb, off, d=y)
         work = "%d rows, 32 experts, N=%d, K=%d" % (R, Ng, Kg)
     elif name == "route":
         logits = torch.randn((4096, 256), device=dev, generator=g)
