@@ -155,6 +155,8 @@ constexpr int kSingleStages = 4;     // one CTA holds all 256 B rows: 48 KB of o
 constexpr int kPairRegsWG0 = 64, kPairRegsPromo = 216;
 static_assert(128 * kPairRegsWG0 + 256 * kPairRegsPromo <= kThreads * 168, "register split");
 
+constexpr int kOutStageWarpBytes = 32 * 64;
+
 template <bool PAIR, int BN, int STAGES, int BMODE, bool GROUPED, bool TWO_ROW = false>
 struct PairLayout {
     static constexpr int kABytes = BM * BK;                      // this CTA's 128 rows
@@ -180,7 +182,11 @@ struct PairLayout {
     static constexpr int kPrivColBytes = BMODE == 1 ? 2 * kPromoWarps * (TWO_ROW ? BN : BN / 2) * 4 : 0;
     static constexpr int kGrpOff = kPrivColOff + kPrivColBytes;
     static constexpr int kGrpBytes = GROUPED ? 2 * (kMaxExperts + 1) * 4 : 0;
-    static constexpr int kBytes = kGrpOff + kGrpBytes;
+    // one-row promotion: each warp's output staging tile (32 rows x 64 bytes);
+    // not with per-column B scales, whose scale buffers leave no room for it
+    static constexpr int kOutStageOff = (kGrpOff + kGrpBytes + 127) & ~127;
+    static constexpr int kOutStageBytes = (TWO_ROW || BMODE == 1) ? 0 : kPromoWarps * kOutStageWarpBytes;
+    static constexpr int kBytes = kOutStageOff + kOutStageBytes;
     static constexpr int kDynSmem = kBytes + 1024;
     static_assert(kABytes % 1024 == 0 && kBBytes % 1024 == 0 && kStageBytes % 1024 == 0,
                   "operand tiles start on 1024-byte boundaries");
@@ -697,7 +703,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             const int64_t m = t.row0 + r;
             const int64_t ncol0 = int64_t(t.n0) + half * kHalf;
-            if (ncol0 < args.N && m < t.row_end && m < args.M) {
+            if (ncol0 < args.N) {                  // N % 128 == 0: the whole half is inside D or outside it
+                const bool row_ok = m < t.row_end && m < args.M;
+                float inv = 1.0f;
                 if constexpr (OUT == kOutE4M3) {
                     // The thread holds row m, columns ncol0 .. ncol0+127 of D in
                     // fp32: exactly one 1x128 activation tile of the next GEMM
@@ -706,36 +714,72 @@ __global__ void __launch_bounds__(kThreads, 1)
                     float amax = 0.0f;
 #pragma unroll
                     for (int i = 0; i < kHalf / 2; ++i) amax = fmaxf(amax, fmaxf(fabsf(acc[i].x), fabsf(acc[i].y)));
-                    float inv;
                     const float sc = tile_scale(amax, (args.flags & FP8_SCALE_POW2) != 0, inv);
-                    uint8_t* dst = reinterpret_cast<uint8_t*>(args.d) + m * args.N + ncol0;
+                    if (row_ok) args.s_out[(ncol0 / 128) * args.M + m] = sc;
+                }
+                if constexpr (L::kOutStageBytes == 0) {
+                    // (per-column B scales, E4M3 out) the thread stores its own row
+                    if (row_ok) {
+                        uint8_t* dst = reinterpret_cast<uint8_t*>(args.d) + m * args.N + ncol0;
 #pragma unroll
-                    for (int i = 0; i < kHalf / 2; i += 8) {
-                        uint32_t w[4];
+                        for (int i = 0; i < kHalf / 2; i += 8) {
+                            uint32_t w[4];
 #pragma unroll
-                        for (int j = 0; j < 4; ++j)
-                            w[j] = cvt_e4m3x2(__fmul_rn(acc[i + 2 * j].x, inv), __fmul_rn(acc[i + 2 * j].y, inv)) |
-                                   (cvt_e4m3x2(__fmul_rn(acc[i + 2 * j + 1].x, inv),
-                                               __fmul_rn(acc[i + 2 * j + 1].y, inv))
-                                    << 16);
-                        *reinterpret_cast<uint4*>(dst + 2 * i) = make_uint4(w[0], w[1], w[2], w[3]);
+                            for (int j = 0; j < 4; ++j)
+                                w[j] = cvt_e4m3x2(__fmul_rn(acc[i + 2 * j].x, inv), __fmul_rn(acc[i + 2 * j].y, inv)) |
+                                       (cvt_e4m3x2(__fmul_rn(acc[i + 2 * j + 1].x, inv),
+                                                   __fmul_rn(acc[i + 2 * j + 1].y, inv))
+                                        << 16);
+                            *reinterpret_cast<uint4*>(dst + 2 * i) = make_uint4(w[0], w[1], w[2], w[3]);
+                        }
                     }
-                    args.s_out[(ncol0 / 128) * args.M + m] = sc;
-                } else if constexpr (OUT == kOutF32) {
-                    float* dst = reinterpret_cast<float*>(args.d) + m * args.N + ncol0;
-#pragma unroll
-                    for (int i = 0; i < kHalf / 2; i += 2)
-                        *reinterpret_cast<float4*>(dst + 2 * i) =
-                            make_float4(acc[i].x, acc[i].y, acc[i + 1].x, acc[i + 1].y);
                 } else {
-                    uint16_t* dst = reinterpret_cast<uint16_t*>(args.d) + m * args.N + ncol0;
+                // The stores go through this warp's staging tile, 64 bytes of
+                // each of its 32 rows at a time (16-byte piece j of row i at
+                // piece j ^ ((i / 2) % 4): conflict-free both ways), so that a
+                // warp's store instruction writes whole 64-byte segments of 8
+                // rows instead of 16 bytes of each of 32 rows.
+                uint8_t* stg = smem + L::kOutStageOff + (warp - 4) * kOutStageWarpBytes;
+                const int64_t m_warp = t.row0 + 32 * wq;
+                constexpr int kElem = OUT == kOutF32 ? 4 : (OUT == kOutBF16 ? 2 : 1);
+                constexpr int kChunkCols = 64 / kElem;
+                const int swz = (lane >> 1) & 3;
 #pragma unroll
-                    for (int i = 0; i < kHalf / 2; i += 4) {
-                        const uint4 o = make_uint4(cvt_bf16x2(acc[i].x, acc[i].y), cvt_bf16x2(acc[i + 1].x, acc[i + 1].y),
-                                                   cvt_bf16x2(acc[i + 2].x, acc[i + 2].y),
-                                                   cvt_bf16x2(acc[i + 3].x, acc[i + 3].y));
-                        *reinterpret_cast<uint4*>(dst + 2 * i) = o;
+                for (int c = 0; c < kHalf / kChunkCols; ++c) {
+                    uint32_t w[16];
+                    if constexpr (OUT == kOutBF16) {
+#pragma unroll
+                        for (int i = 0; i < 16; ++i) w[i] = cvt_bf16x2(acc[c * 16 + i].x, acc[c * 16 + i].y);
+                    } else if constexpr (OUT == kOutF32) {
+#pragma unroll
+                        for (int i = 0; i < 8; ++i) {
+                            w[2 * i] = __float_as_uint(acc[c * 8 + i].x);
+                            w[2 * i + 1] = __float_as_uint(acc[c * 8 + i].y);
+                        }
+                    } else {
+#pragma unroll
+                        for (int i = 0; i < 16; ++i) {
+                            const float2 p0 = acc[c * 32 + 2 * i], p1 = acc[c * 32 + 2 * i + 1];
+                            w[i] = cvt_e4m3x2(__fmul_rn(p0.x, inv), __fmul_rn(p0.y, inv)) |
+                                   (cvt_e4m3x2(__fmul_rn(p1.x, inv), __fmul_rn(p1.y, inv)) << 16);
+                        }
                     }
+#pragma unroll
+                    for (int j = 0; j < 4; ++j)
+                        *reinterpret_cast<uint4*>(stg + lane * 64 + ((j ^ swz) << 4)) =
+                            make_uint4(w[4 * j], w[4 * j + 1], w[4 * j + 2], w[4 * j + 3]);
+                    __syncwarp();
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        const int rr = 8 * i + (lane >> 2), pc = lane & 3;
+                        const uint4 v = *reinterpret_cast<const uint4*>(stg + rr * 64 + ((pc ^ ((rr >> 1) & 3)) << 4));
+                        const int64_t mm = m_warp + rr;
+                        if (mm < t.row_end && mm < args.M)
+                            *reinterpret_cast<uint4*>(reinterpret_cast<uint8_t*>(args.d) +
+                                                      (mm * args.N + ncol0 + c * kChunkCols) * kElem + pc * 16) = v;
+                    }
+                    __syncwarp();
+                }
                 }
             }
         }
