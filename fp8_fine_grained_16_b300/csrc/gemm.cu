@@ -184,7 +184,7 @@ struct PairLayout {
     static constexpr int kGrpBytes = GROUPED ? 2 * (kMaxExperts + 1) * 4 : 0;
     // one-row promotion: each warp's output staging tile (32 rows x 64 bytes);
     // not with per-column B scales, whose scale buffers leave no room for it
-    static constexpr int kOutStageOff = (kGrpOff + kGrpBytes + 127) & ~127;
+    static constexpr int kOutStageOff = (kGrpOff + kGrpBytes + 1023) & ~1023;
     static constexpr int kOutStageBytes = (TWO_ROW || BMODE == 1) ? 0 : kPromoWarps * kOutStageWarpBytes;
     static constexpr int kBytes = kOutStageOff + kOutStageBytes;
     static constexpr int kDynSmem = kBytes + 1024;
@@ -233,7 +233,7 @@ template <bool PAIR, int BN, int STAGES, int BMODE, int OUT, bool GROUPED>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                      const __grid_constant__ CUtensorMap tmSA, const __grid_constant__ CUtensorMap tmSB,
-                     const GemmArgs args) {
+                     const __grid_constant__ CUtensorMap tmD, const GemmArgs args) {
     // Per-column B scales (BMODE 1, bf16/fp32 out): the two-row promotion
     constexpr bool kTwoRow = two_row_promotion(BMODE, OUT);
     using L = PairLayout<PAIR, BN, STAGES, BMODE, GROUPED, kTwoRow>;
@@ -736,11 +736,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                 } else {
                 // The stores go through this warp's staging tile, 64 bytes of
                 // each of its 32 rows at a time (16-byte piece j of row i at
-                // piece j ^ ((i / 2) % 4): conflict-free both ways), so that a
-                // warp's store instruction writes whole 64-byte segments of 8
-                // rows instead of 16 bytes of each of 32 rows.
+                // piece j ^ ((i / 2) % 4), the 64-byte swizzle of the tensor
+                // map of D: conflict-free both ways).  A warp whose 32 rows all
+                // belong to the tile hands each chunk to one TMA tensor store;
+                // at the end of an expert or of D the lanes store the rows that
+                // belong, 64-byte segments of 8 rows per instruction.
                 uint8_t* stg = smem + L::kOutStageOff + (warp - 4) * kOutStageWarpBytes;
                 const int64_t m_warp = t.row0 + 32 * wq;
+                const bool whole = m_warp + 32 <= t.row_end && m_warp + 32 <= args.M;     // warp-uniform
                 constexpr int kElem = OUT == kOutF32 ? 4 : (OUT == kOutBF16 ? 2 : 1);
                 constexpr int kChunkCols = 64 / kElem;
                 const int swz = (lane >> 1) & 3;
@@ -764,24 +767,42 @@ __global__ void __launch_bounds__(kThreads, 1)
                                    (cvt_e4m3x2(__fmul_rn(p1.x, inv), __fmul_rn(p1.y, inv)) << 16);
                         }
                     }
+                    // the previous tensor store out of the staging tile has read it
+                    if (lane == 0) bulk_wait_group_read0();
+                    __syncwarp();
 #pragma unroll
                     for (int j = 0; j < 4; ++j)
                         *reinterpret_cast<uint4*>(stg + lane * 64 + ((j ^ swz) << 4)) =
                             make_uint4(w[4 * j], w[4 * j + 1], w[4 * j + 2], w[4 * j + 3]);
-                    __syncwarp();
+                    if (whole) {
+                        fence_proxy_async_smem();
+                        __syncwarp();
+                        if (lane == 0) {
+                            tma_store_2d(&tmD, stg, int32_t(ncol0 + c * kChunkCols), int32_t(m_warp));
+                            bulk_commit_group();
+                        }
+                    } else {
+                        __syncwarp();
 #pragma unroll
-                    for (int i = 0; i < 4; ++i) {
-                        const int rr = 8 * i + (lane >> 2), pc = lane & 3;
-                        const uint4 v = *reinterpret_cast<const uint4*>(stg + rr * 64 + ((pc ^ ((rr >> 1) & 3)) << 4));
-                        const int64_t mm = m_warp + rr;
-                        if (mm < t.row_end && mm < args.M)
-                            *reinterpret_cast<uint4*>(reinterpret_cast<uint8_t*>(args.d) +
-                                                      (mm * args.N + ncol0 + c * kChunkCols) * kElem + pc * 16) = v;
+                        for (int i = 0; i < 4; ++i) {
+                            const int rr = 8 * i + (lane >> 2), pc = lane & 3;
+                            const uint4 v =
+                                *reinterpret_cast<const uint4*>(stg + rr * 64 + ((pc ^ ((rr >> 1) & 3)) << 4));
+                            const int64_t mm = m_warp + rr;
+                            if (mm < t.row_end && mm < args.M)
+                                *reinterpret_cast<uint4*>(reinterpret_cast<uint8_t*>(args.d) +
+                                                          (mm * args.N + ncol0 + c * kChunkCols) * kElem + pc * 16) = v;
+                        }
+                        __syncwarp();
                     }
-                    __syncwarp();
                 }
                 }
             }
+        }
+        // this warp's tensor stores are complete before the CTA can leave
+        if constexpr (L::kOutStageBytes > 0) {
+            if (lane == 0) bulk_wait_group0();
+            __syncwarp();
         }
         if (!ok) record_status(FP8_ERR_TIMEOUT);
         }
@@ -853,11 +874,30 @@ static int64_t split_workspace_bytes(int sms, int64_t K) {
     return K / 128 >= kSplitMinKBlocks ? int64_t(sms / 2) * kSlabBytes : 0;
 }
 
+// D [rows][N] as boxes of 32 rows x 64 bytes with the 64-byte swizzle: the
+// epilogue's tensor stores from its staging tiles.
+static bool make_out_map(CUtensorMap* map, void* d, int64_t rows, int64_t N, int out) {
+    auto fn = encode_fn();
+    if (!fn) return false;
+    const int elem = out == kOutF32 ? 4 : (out == kOutBF16 ? 2 : 1);
+    const CUtensorMapDataType dt = out == kOutF32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32
+                                                  : (out == kOutBF16 ? CU_TENSOR_MAP_DATA_TYPE_UINT16
+                                                                     : CU_TENSOR_MAP_DATA_TYPE_UINT8);
+    cuuint64_t dims[2] = {cuuint64_t(N), cuuint64_t(rows)};
+    cuuint64_t strides[1] = {cuuint64_t(N) * cuuint64_t(elem)};
+    cuuint32_t box[2] = {cuuint32_t(64 / elem), 32u};
+    cuuint32_t estr[2] = {1u, 1u};
+    return fn(map, dt, 2u, d, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B,
+              CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 template <bool PAIR, int BN, int STAGES, int BMODE, int OUT, bool GROUPED>
 static int launch_pair(const CUtensorMap& ma, const CUtensorMap& mb, const CUtensorMap& msa, const CUtensorMap& msb,
                        GemmArgs args, int sms, cudaStream_t stream, int64_t ws_bytes = 0) {
     using L = PairLayout<PAIR, BN, STAGES, BMODE, GROUPED, two_row_promotion(BMODE, OUT)>;
     auto kern = gemm_pair_kernel<PAIR, BN, STAGES, BMODE, OUT, GROUPED>;
+    CUtensorMap md;
+    if (!make_out_map(&md, args.d, args.M, args.N, OUT)) return FP8_ERR_CUDA;
     static unsigned char smem_opted_in[kMaxDevices] = {};
     if (!opt_in_dynamic_smem(kern, L::kDynSmem, smem_opted_in)) return FP8_ERR_CUDA;
     cudaLaunchConfig_t cfg = {};
@@ -872,7 +912,7 @@ static int launch_pair(const CUtensorMap& ma, const CUtensorMap& mb, const CUten
     if constexpr (!PAIR) {
         // one CTA per SM (shared memory and launch bounds allow no more)
         cfg.gridDim = dim3(sms);
-        if (cudaLaunchKernelEx(&cfg, kern, ma, mb, msa, msb, args) != cudaSuccess) return FP8_ERR_CUDA;
+        if (cudaLaunchKernelEx(&cfg, kern, ma, mb, msa, msb, md, args) != cudaSuccess) return FP8_ERR_CUDA;
         return cudaGetLastError() == cudaSuccess ? FP8_OK : FP8_ERR_CUDA;
     }
     cfg.attrs = attr;
@@ -896,7 +936,7 @@ static int launch_pair(const CUtensorMap& ma, const CUtensorMap& mb, const CUten
         clusters = int(plan.pairs);
     }
     cfg.gridDim = dim3(2 * clusters);
-    if (cudaLaunchKernelEx(&cfg, kern, ma, mb, msa, msb, args) != cudaSuccess) return FP8_ERR_CUDA;
+    if (cudaLaunchKernelEx(&cfg, kern, ma, mb, msa, msb, md, args) != cudaSuccess) return FP8_ERR_CUDA;
     if constexpr (PAIR && !GROUPED) {
         if (args.split > 0) {
             const unsigned blocks = unsigned(n_tail * (2 * BM / kFixRowsPerBlock));

@@ -31,22 +31,6 @@
 
 namespace fp8bs {
 
-// Tensor store from this CTA's shared memory (the box of `map` at (c0, c1)),
-// tracked by the issuing thread's bulk-async groups.
-FP8_DEV void tma_store_2d(const CUtensorMap* map, const void* src, int32_t c0, int32_t c1) {
-    asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%2, %3}], [%1];" ::"l"(
-                     reinterpret_cast<uint64_t>(map)),
-                 "r"(smem_u32(src)), "r"(c0), "r"(c1)
-                 : "memory");
-}
-FP8_DEV void bulk_commit_group() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
-// every committed store of this thread has finished reading shared memory
-FP8_DEV void bulk_wait_group_read0() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
-// every committed store of this thread is complete
-FP8_DEV void bulk_wait_group0() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
-// shared-memory writes of this thread made visible to the async proxy (TMA)
-FP8_DEV void fence_proxy_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
-
 __device__ int g_tr_status;
 FP8_DEV void tr_record(int code) { atomicCAS(&g_tr_status, 0, code); }
 
