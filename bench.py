@@ -386,30 +386,44 @@ def gemm_launches(F, m, n, k, dev) -> int:
 class _SmClock:
     """The SM clock read through NVML right after each timed repetition, so
     that every row carries the clock it ran at (a row measured at a lower
-    clock -- the power cap acting after the heavy rows -- shows as such)."""
+    clock -- the power cap acting after the heavy rows -- shows as such).
+    NVML comes from pynvml if installed, else from the driver's
+    libnvidia-ml.so.1 through ctypes; without either, one nvidia-smi query
+    per row stands in."""
 
     def __init__(self):
         self.h = None
         self.last = None
         self.index = torch.cuda.current_device()
+        self.read = lambda: None
         try:
             import pynvml
             pynvml.nvmlInit()
-            self.nv = pynvml
-            self.h = pynvml.nvmlDeviceGetHandleByIndex(self.index)
+            h = pynvml.nvmlDeviceGetHandleByIndex(self.index)
+            self.read = lambda: float(pynvml.nvmlDeviceGetClockInfo(h, pynvml.NVML_CLOCK_SM))
+            self.h = h
+            return
+        except Exception:
+            pass
+        try:
+            import ctypes
+            nv = ctypes.CDLL("libnvidia-ml.so.1")
+            if nv.nvmlInit_v2() != 0:
+                raise OSError("nvmlInit_v2 failed")
+            h = ctypes.c_void_p()
+            if nv.nvmlDeviceGetHandleByIndex_v2(ctypes.c_uint(self.index), ctypes.byref(h)) != 0:
+                raise OSError("nvmlDeviceGetHandleByIndex_v2 failed")
+            clk = ctypes.c_uint()
+
+            def read():
+                # NVML_CLOCK_SM = 1
+                return float(clk.value) if nv.nvmlDeviceGetClockInfo(h, 1, ctypes.byref(clk)) == 0 else None
+
+            self.read = read
+            self.h = h
         except Exception as e:               # fall back to one nvidia-smi query per row
             sys.stderr.write("NVML unavailable (%s); row clocks from nvidia-smi\n" % e)
             self.h = None
-
-    def read(self):
-        if self.h is None:
-            return None
-        try:
-            return float(self.nv.nvmlDeviceGetClockInfo(self.h, self.nv.NVML_CLOCK_SM))
-        except Exception as e:
-            sys.stderr.write("NVML clock read failed (%s); row clocks from nvidia-smi\n" % e)
-            self.h = None
-            return None
 
     def query(self):
         """One nvidia-smi reading of the SM clock (MHz), or None."""
@@ -424,7 +438,7 @@ class _SmClock:
 _SM_CLOCK = None
 
 
-def timed_reps(fn, reps, flush, stream):
+def timed_reps(fn, reps, flush, stream, clocks=None):
     """Device times (ms) of `reps` runs of fn, each timed alone: the GPU is
     synchronised after every run (so each starts from an idle GPU at its
     burst clock) and L2 is flushed before it.  Between the flush and the
@@ -442,6 +456,8 @@ def timed_reps(fn, reps, flush, stream):
         b.record(stream)
         b.synchronize()
         ts.append(a.elapsed_time(b))
+        if clocks is not None:
+            clocks.append(_SM_CLOCK.read() if _SM_CLOCK is not None else None)
     return ts
 
 
@@ -451,11 +467,15 @@ def _time(fn, reps, warm, flush, stream):
     global _SM_CLOCK
     if _SM_CLOCK is None:
         _SM_CLOCK = _SmClock()
+    # a short idle first, so that a row does not start under the power cap
+    # the rows before it drove the part into
+    time.sleep(0.3)
     for _ in range(warm):
         fn()
-    ts = timed_reps(fn, reps, flush, stream)
-    c = _SM_CLOCK.read()
-    _SM_CLOCK.last = c if c is not None else _SM_CLOCK.query()
+    mhz = []
+    ts = timed_reps(fn, reps, flush, stream, mhz)
+    mhz = [c for c in mhz if c is not None]
+    _SM_CLOCK.last = statistics.median(mhz) if mhz else _SM_CLOCK.query()
     return statistics.median(ts)
 
 

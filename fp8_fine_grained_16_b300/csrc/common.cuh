@@ -162,6 +162,8 @@ FP8_DEV void tma_store_2d(const CUtensorMap* map, const void* src, int32_t c0, i
 FP8_DEV void bulk_commit_group() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
 // every committed store of this thread has finished reading shared memory
 FP8_DEV void bulk_wait_group_read0() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
+// all but the most recent committed store of this thread have finished reading shared memory
+FP8_DEV void bulk_wait_group_read1() { asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory"); }
 // every committed store of this thread is complete
 FP8_DEV void bulk_wait_group0() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
 // shared-memory writes of this thread made visible to the async proxy (TMA)

@@ -25,7 +25,7 @@
 //
 //   warp 0        TMA producer: A and B halves (128-byte swizzle) and the
 //                 scales the promotion needs (sA of the CTA's 128 rows, sB of
-//                 the tile's columns) into a 6-stage ring (4 alone).
+//                 the tile's columns) into a 4-stage ring.
 //   warp 1        allocates the pair's TMEM (two 256-column fp32
 //                 accumulators); in the leader CTA it issues four MMAs
 //                 (K = 32 each) per K block and commits them to both CTAs'
@@ -145,7 +145,7 @@ struct Tile {
 //                        MMA commit of that K block (its accumulator is ready).
 //   empty[s] (each)    = MMA commit + this CTA's 8 promotion warps (each
 //                        arrives once it has copied the scales it reads).
-constexpr int kPairStages = 6;
+constexpr int kPairStages = 4;
 constexpr int kSingleStages = 4;     // one CTA holds all 256 B rows: 48 KB of operands per stage
 // Register split (launched with 168 per thread, 64512 in all): warpgroup 0
 // keeps 64 (the producer's per-K-block state spills at 40), the promotion
@@ -155,7 +155,7 @@ constexpr int kSingleStages = 4;     // one CTA holds all 256 B rows: 48 KB of o
 constexpr int kPairRegsWG0 = 64, kPairRegsPromo = 216;
 static_assert(128 * kPairRegsWG0 + 256 * kPairRegsPromo <= kThreads * 168, "register split");
 
-constexpr int kOutStageWarpBytes = 32 * 64;
+constexpr int kOutStageChunk = 32 * 64;                 // one staging tile: 32 rows x 64 bytes
 
 template <bool PAIR, int BN, int STAGES, int BMODE, bool GROUPED, bool TWO_ROW = false>
 struct PairLayout {
@@ -185,7 +185,11 @@ struct PairLayout {
     // one-row promotion: each warp's output staging tile (32 rows x 64 bytes);
     // not with per-column B scales, whose scale buffers leave no room for it
     static constexpr int kOutStageOff = (kGrpOff + kGrpBytes + 1023) & ~1023;
-    static constexpr int kOutStageBytes = (TWO_ROW || BMODE == 1) ? 0 : kPromoWarps * kOutStageWarpBytes;
+    // two staging tiles per warp (alternating by chunk) where they fit, else one
+    static constexpr int kOutStageBufs =
+        (TWO_ROW || BMODE == 1) ? 0 : (kOutStageOff + 2 * kPromoWarps * kOutStageChunk + 1024 <= 232448 ? 2 : 1);
+    static constexpr int kOutStageWarpBytes = kOutStageBufs * kOutStageChunk;
+    static constexpr int kOutStageBytes = kPromoWarps * kOutStageWarpBytes;
     static constexpr int kBytes = kOutStageOff + kOutStageBytes;
     static constexpr int kDynSmem = kBytes + 1024;
     static_assert(kABytes % 1024 == 0 && kBBytes % 1024 == 0 && kStageBytes % 1024 == 0,
@@ -741,7 +745,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 // belong to the tile hands each chunk to one TMA tensor store;
                 // at the end of an expert or of D the lanes store the rows that
                 // belong, 64-byte segments of 8 rows per instruction.
-                uint8_t* stg = smem + L::kOutStageOff + (warp - 4) * kOutStageWarpBytes;
+                uint8_t* const stg_warp = smem + L::kOutStageOff + (warp - 4) * L::kOutStageWarpBytes;
                 const int64_t m_warp = t.row0 + 32 * wq;
                 const bool whole = m_warp + 32 <= t.row_end && m_warp + 32 <= args.M;     // warp-uniform
                 constexpr int kElem = OUT == kOutF32 ? 4 : (OUT == kOutBF16 ? 2 : 1);
@@ -749,6 +753,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int swz = (lane >> 1) & 3;
 #pragma unroll
                 for (int c = 0; c < kHalf / kChunkCols; ++c) {
+                    uint8_t* stg = stg_warp + (c % L::kOutStageBufs) * kOutStageChunk;
                     uint32_t w[16];
                     if constexpr (OUT == kOutBF16) {
 #pragma unroll
@@ -767,8 +772,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                                    (cvt_e4m3x2(__fmul_rn(p1.x, inv), __fmul_rn(p1.y, inv)) << 16);
                         }
                     }
-                    // the previous tensor store out of the staging tile has read it
-                    if (lane == 0) bulk_wait_group_read0();
+                    // the tensor store that last used this staging tile has read it
+                    // (with two tiles, the most recent store may still be reading the other)
+                    if (lane == 0) {
+                        if constexpr (L::kOutStageBufs == 2) bulk_wait_group_read1(); else bulk_wait_group_read0();
+                    }
                     __syncwarp();
 #pragma unroll
                     for (int j = 0; j < 4; ++j)
