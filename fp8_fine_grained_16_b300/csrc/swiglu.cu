@@ -19,20 +19,18 @@
 // One warp per row; each half-warp quantises 128-column tiles (16 lanes x 8
 // values, 16-byte loads of gate and up; two tiles' loads in flight), the
 // amax reduced with shuffles.  Pairs of elements go through two-lane packed
-// fp32 operations, lane by lane the same IEEE operations.
+// fp32 operations, lane by lane the same IEEE operations.  A lane whose 8
+// gates all satisfy |g| <= 87 skips the range handling (the clamps, the +inf
+// select and the reciprocal's fallback test), which cannot change any value
+// there; the rest take the full steps.
 #include "common.cuh"
 
 namespace fp8bs {
 
-// d = 1 + e^x of two values, for sigma = 1/d in the fp32 SwiGLU above, with
-// two-lane packed fp32 operations (each lane is the same IEEE operation as
-// its scalar form).  The definition takes e^x = +inf above 88 and 0 below
-// -87.  Inputs in [-87, 88] take the steps unchanged.  An input below -87 is
-// computed at -87: e^-87 ~ 1.6e-38 is far below half an ulp of 1, so 1 + e
-// rounds to exactly 1, the d that e = 0 gives, and no select is needed for
-// it.  An input above 88 is computed at 88 and its e replaced by +inf.
-FP8_DEV float2 one_plus_exp(float2 x) {
-    const float2 xc = make_float2(fminf(fmaxf(x.x, -87.0f), 88.0f), fminf(fmaxf(x.y, -87.0f), 88.0f));
+// The reduction and polynomial steps of e^x for two values already in
+// [-87, 88]: returns 2^n * P(r), with n = rint(x * log2 e), r = x - n*ln2 (ln2
+// in two parts) and P the degree-7 Taylor polynomial of e^r in Horner form.
+FP8_DEV float2 exp_steps(float2 xc) {
     const float2 t = __fmul2_rn(xc, make_float2(0x1.715476p+0f, 0x1.715476p+0f));   // x * log2(e)
     // t to the nearest integer (ties to even, as rint): adding 1.5 * 2^23 leaves
     // the rounded integer in the low mantissa bits of the sum (|t| < 128), and
@@ -55,24 +53,32 @@ FP8_DEV float2 one_plus_exp(float2 x) {
     // 2^n, n in [-126, 127]: the sum's bits are 0x4B400000 + n, so its bits
     // shifted up by 23 (0x4B400000 << 23 vanishes mod 2^32) plus 127 << 23
     // are those of 2^n
-    const float2 e = __fmul2_rn(p, make_float2(__int_as_float((__float_as_int(big.x) << 23) + (127 << 23)),
-                                                __int_as_float((__float_as_int(big.y) << 23) + (127 << 23))));
+    return __fmul2_rn(p, make_float2(__int_as_float((__float_as_int(big.x) << 23) + (127 << 23)),
+                                     __int_as_float((__float_as_int(big.y) << 23) + (127 << 23))));
+}
+
+// d = 1 + e^x of two values, for sigma = 1/d in the fp32 SwiGLU above, with
+// two-lane packed fp32 operations (each lane is the same IEEE operation as
+// its scalar form).  The definition takes e^x = +inf above 88 and 0 below
+// -87.  Inputs in [-87, 88] take the steps unchanged.  An input below -87 is
+// computed at -87: e^-87 ~ 1.6e-38 is far below half an ulp of 1, so 1 + e
+// rounds to exactly 1, the d that e = 0 gives, and no select is needed for
+// it.  An input above 88 is computed at 88 and its e replaced by +inf.
+FP8_DEV float2 one_plus_exp(float2 x) {
+    const float2 xc = make_float2(fminf(fmaxf(x.x, -87.0f), 88.0f), fminf(fmaxf(x.y, -87.0f), 88.0f));
+    const float2 e = exp_steps(xc);
     const float inf = __int_as_float(0x7F800000);
     return __fadd2_rn(make_float2(1.0f, 1.0f), make_float2(x.x > 88.0f ? inf : e.x, x.y > 88.0f ? inf : e.y));
 }
 
-// The correctly rounded reciprocal 1/d of two values d >= 1 (the IEEE
-// quotient), by Markstein's method (P. Markstein, "Computation of elementary
-// functions on the IBM RISC System/6000 processor", IBM J. Res. Dev. 34(1),
-// 1990): from an approximation y within one ulp of 1/d, the residual
-// r = 1 - d*y is exact in one fused multiply-add and y + r*y, rounded once,
-// is the correctly rounded 1/d.  The approximation is the hardware's
-// rcp.approx.ftz.f32 (at most one ulp off).  Reciprocals below the normal
-// range (d >= 2^126), d = +inf and NaN take __frcp_rn instead, which is what
-// every other d matches bit for bit (checked for all d >= 1 by
-// fp8_selftest_reciprocal).
-FP8_DEV float2 rcp_rn_from_one(float2 d) {
-    if (!(d.x < 0x1p126f && d.y < 0x1p126f)) return make_float2(__frcp_rn(d.x), __frcp_rn(d.y));
+// 1/d correctly rounded for two values d in [1, 2^126) (the IEEE quotient),
+// by Markstein's method (P. Markstein, "Computation of elementary functions
+// on the IBM RISC System/6000 processor", IBM J. Res. Dev. 34(1), 1990):
+// from an approximation y within one ulp of 1/d, the residual r = 1 - d*y is
+// exact in one fused multiply-add and y + r*y, rounded once, is the correctly
+// rounded 1/d.  The approximation is the hardware's rcp.approx.ftz.f32 (at
+// most one ulp off).
+FP8_DEV float2 rcp_rn_markstein(float2 d) {
     float2 y;
     asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(y.x) : "f"(d.x));
     asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(y.y) : "f"(d.y));
@@ -80,11 +86,30 @@ FP8_DEV float2 rcp_rn_from_one(float2 d) {
     return __ffma2_rn(r, y, y);
 }
 
+// 1/d correctly rounded for two values d >= 1: Markstein's method where the
+// reciprocal is normal; d >= 2^126 (results below the normal range), +inf and
+// NaN take __frcp_rn, which every other d matches bit for bit (checked for all
+// d >= 1 by fp8_selftest_reciprocal).
+FP8_DEV float2 rcp_rn_from_one(float2 d) {
+    if (!(d.x < 0x1p126f && d.y < 0x1p126f)) return make_float2(__frcp_rn(d.x), __frcp_rn(d.y));
+    return rcp_rn_markstein(d);
+}
+
 // (g * sigma(g)) * u for two elements, sigma(g) = 1 / (1 + e^-g); the
 // reciprocal is the correctly rounded one, equal to the IEEE quotient.
 FP8_DEV float2 swiglu2_fp32(float2 g, float2 u) {
     const float2 d = one_plus_exp(make_float2(-g.x, -g.y));
     const float2 sig = rcp_rn_from_one(d);
+    return __fmul2_rn(__fmul2_rn(g, sig), u);
+}
+
+// The same h for two gates with |g| <= 87, without the range handling, which
+// cannot change anything there: x = -g lies in [-87, 87], so the clamps leave
+// it as it is and the +inf select does not fire, and d <= 1 + e^87 < 2^126,
+// so Markstein's reciprocal needs no fallback.
+FP8_DEV float2 swiglu2_fp32_in_range(float2 g, float2 u) {
+    const float2 d = __fadd2_rn(make_float2(1.0f, 1.0f), exp_steps(make_float2(-g.x, -g.y)));
+    const float2 sig = rcp_rn_markstein(d);
     return __fmul2_rn(__fmul2_rn(g, sig), u);
 }
 
@@ -139,12 +164,23 @@ __global__ void __launch_bounds__(256) swiglu_quant_1x128_kernel(const uint16_t*
             if (live) {
                 const uint32_t gw[4] = {gv[u].x, gv[u].y, gv[u].z, gv[u].w};
                 const uint32_t uw[4] = {uv[u].x, uv[u].y, uv[u].z, uv[u].w};
+                float2 g[4], uu[4];
+                bool in_range = true;          // |g| <= 87 for all 8 gates (false for NaN)
 #pragma unroll
                 for (int j = 0; j < 4; ++j) {
-                    h[j] = swiglu2_fp32(make_float2(bf16_lo(gw[j]), bf16_hi(gw[j])),
-                                        make_float2(bf16_lo(uw[j]), bf16_hi(uw[j])));
-                    amax = fmaxf(amax, fmaxf(fabsf(h[j].x), fabsf(h[j].y)));
+                    g[j] = make_float2(bf16_lo(gw[j]), bf16_hi(gw[j]));
+                    uu[j] = make_float2(bf16_lo(uw[j]), bf16_hi(uw[j]));
+                    in_range &= (fabsf(g[j].x) <= 87.0f) & (fabsf(g[j].y) <= 87.0f);
                 }
+                if (in_range) {
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) h[j] = swiglu2_fp32_in_range(g[j], uu[j]);
+                } else {
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) h[j] = swiglu2_fp32(g[j], uu[j]);
+                }
+#pragma unroll
+                for (int j = 0; j < 4; ++j) amax = fmaxf(amax, fmaxf(fabsf(h[j].x), fabsf(h[j].y)));
             }
             // amax of the tile: xor offsets below 16 stay inside the half-warp
 #pragma unroll
