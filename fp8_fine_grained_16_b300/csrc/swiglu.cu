@@ -134,7 +134,7 @@ constexpr int kSgRows = 8;          // rows (warps) per CTA
 constexpr int kSgTiles = 2;         // tiles per half-warp per iteration (loads in flight)
 
 template <bool POW2>
-__global__ void __launch_bounds__(256) swiglu_quant_1x128_kernel(const uint16_t* __restrict__ y, int64_t R, int64_t I,
+__global__ void __launch_bounds__(256, 5) swiglu_quant_1x128_kernel(const uint16_t* __restrict__ y, int64_t R, int64_t I,
                                                                   int64_t ldy, uint8_t* __restrict__ q,
                                                                   float* __restrict__ s) {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
