@@ -106,3 +106,42 @@ def test_moe_up_pow2_full_sampled(fb, orc):
             cols = np.arange(nb * 128, (nb + 1) * 128)
             ref = orc.gemm_blockscaled(par[lo:hi], np.ascontiguousarray(spr[:, lo:hi]), qb[cols], sbb[nb:nb + 1], 0)
             assert_gemm_close(got[lo:hi, nb * 128:(nb + 1) * 128], ref, True, orc, "moe_up pow2 e=%d nb=%d" % (e, nb))
+
+
+def test_moe_down_pow2_full_sampled(fb, orc):
+    """The down-projection workload (256 experts, top-8 of 4096 tokens,
+    K = 2048) with power-of-two scales: h quantised 1x128 to powers of two,
+    grouped GEMM N = 7168 on the microscaled MMA; four experts (the first, the
+    last, the largest and one in the middle) checked against the oracle on the
+    first and last column blocks."""
+    T, E, k, N, K = 4096, 256, 8, 7168, 2048
+    P = fb.FP8_SCALE_POW2
+    d = S.moe_down(with_weights=False)
+    h, logits = d["h"], d["logits"]
+    r = fb.fp8_moe_route_topk(logits.cuda(), k)
+    ref_route = orc.route_topk(logits.numpy(), k)
+    assert_same_bits(r["off"], ref_route["off"], "off")
+    qh, sh = fb.fp8_quant_act_1x128(h.cuda(), flags=P)
+    qhr, shr = orc.quant_act_1x128(S.bf16_bits(h), P)
+    assert_same_bits(qh, qhr, "down-projection input codes")
+    assert_same_bits(sh, shr, "down-projection input scales")
+    w = S.expert_weights(1, E, N, K, device="cuda")
+    qw, sw = fb.fp8_quant_weight_128x128(w, flags=P)
+    del w
+    y = fb.fp8_grouped_gemm_blockscaled_pow2(qh, sh, qw, sw, r["off"])
+    assert fb.fp8_get_status() == 0
+    off = ref_route["off"]
+    counts = np.diff(off)
+    got = to_np(y)
+    for e in sorted({0, 255, int(np.argmax(counts)), 131}):
+        lo, hi = int(off[e]), int(off[e + 1])
+        if hi == lo:
+            continue
+        wb = S.bf16_bits(S.expert_weight(1, e, N, K, device="cuda"))
+        qb, sbb = orc.quant_weight_128x128(wb, P)
+        assert_same_bits(qw[e], qb, "expert %d codes" % e)
+        for nb in (0, N // 128 - 1):
+            cols = np.arange(nb * 128, (nb + 1) * 128)
+            ref = orc.gemm_blockscaled(qhr[lo:hi], np.ascontiguousarray(shr[:, lo:hi]), qb[cols], sbb[nb:nb + 1], 0)
+            assert_gemm_close(got[lo:hi, nb * 128:(nb + 1) * 128], ref, True, orc,
+                              "moe_down pow2 e=%d nb=%d" % (e, nb))

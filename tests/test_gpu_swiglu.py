@@ -120,3 +120,31 @@ def test_reciprocal_matches_frcp_rn_for_every_d_from_one(fb):
     approximation) equals __frcp_rn bit for bit for every float d >= 1, +inf
     and every NaN pattern: all 2^30 + 2^23 bit patterns from 0x3F800000."""
     assert fb.fp8_selftest_reciprocal(0x3F800000, 0x7FFFFFFF) == 0
+
+
+def test_swiglu_quant_gates_at_the_range_boundary_bit_exact(fb, orc):
+    """Gates at |g| = 87 (the largest value the in-range steps take), the next
+    bf16 values past it (87.5, 88, 88.5) and NaN-free extremes, scattered so
+    that some lanes' 8 gates are all in range and others hold one gate just
+    outside; codes and scales bit for bit against the oracle, both scale
+    modes."""
+    R, I = 96, 512
+    y = _bf16((R, 2 * I), 31, 2.0).float()
+    g = torch.Generator().manual_seed(32)
+    edge = torch.tensor([87.0, -87.0, 87.5, -87.5, 88.0, -88.0, 88.5, -88.5, 86.5, -86.5])
+    for r in range(R):
+        n = int(torch.randint(0, 4, (1,), generator=g))        # 0..3 edge gates in this row
+        cols = torch.randint(0, I, (n,), generator=g)
+        vals = edge[torch.randint(0, len(edge), (n,), generator=g)]
+        y[r, cols] = vals
+    y[0, :8] = 87.0                                             # a lane all at the boundary
+    y[1, 8:16] = -87.0
+    y[2, 16:23] = 1.0
+    y[2, 23] = 87.5                                             # one gate past it in a lane
+    y = y.to(torch.bfloat16)
+    for flags in (1, 0):
+        q, s = fb.fp8_swiglu_quant_1x128(y.cuda(), I, flags=flags)
+        torch.cuda.synchronize()
+        q_ref, s_ref = orc.swiglu_quant_1x128(S.bf16_bits(y), I, flags)
+        assert_same_bits(q, q_ref, "boundary codes flags%d" % flags)
+        assert_same_bits(s, s_ref, "boundary scales flags%d" % flags)
