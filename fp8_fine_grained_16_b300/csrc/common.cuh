@@ -54,6 +54,32 @@ FP8_DEV float tile_scale(float amax, bool pow2, float& inv) {
     return __uint_as_float(uint32_t(127 + e) << 23);
 }
 
+// ---------------------------------------------------------------- dependent launches
+// A kernel launched with programmatic stream serialisation (launch_pdl, or
+// the GEMMs' own launches) may start while the kernel before it on the stream
+// is still running; it must call pdl_wait() before it reads anything that
+// kernel writes (the wait returns once that kernel has completed and its
+// writes are visible; in a kernel launched without the attribute it returns
+// at once).  pdl_launch_dependents() lets the next such kernel start early.
+FP8_DEV void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+FP8_DEV void pdl_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
+                              Args... args) {
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, static_cast<KArgs>(args)...);
+}
+
 // ---------------------------------------------------------------- misc PTX
 FP8_DEV uint32_t smem_u32(const void* p) {
     return static_cast<uint32_t>(__cvta_generic_to_shared(p));

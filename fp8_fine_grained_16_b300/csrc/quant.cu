@@ -40,13 +40,12 @@ constexpr int kQ1Rows = 8;      // rows (warps) per CTA
 constexpr int kQ1U = 4;         // warp steps (tile pairs) unrolled per iteration
 
 template <bool POW2>
-__global__ void __launch_bounds__(256) quant_act_1x128_kernel(const uint16_t* __restrict__ x, int64_t M, int64_t K,
-                                                              int64_t ldx, uint8_t* __restrict__ q,
-                                                              float* __restrict__ s) {
+FP8_DEV void quant_act_1x128_rows(const uint16_t* __restrict__ x, int64_t M, int64_t K, int64_t ldx,
+                                  uint8_t* __restrict__ q, float* __restrict__ s, int64_t cta) {
     const int lane = threadIdx.x & 31;
     const int half = lane >> 4;
     const int l16 = lane & 15;
-    const int64_t m = int64_t(blockIdx.x) * kQ1Rows + (threadIdx.x >> 5);
+    const int64_t m = cta * kQ1Rows + (threadIdx.x >> 5);
     if (m >= M) return;                                   // warp-uniform
     const int nkb = int(K >> 7);
     const uint4* xr = reinterpret_cast<const uint4*>(x + m * ldx) + l16;   // + 16 * kb per tile
@@ -89,17 +88,23 @@ __global__ void __launch_bounds__(256) quant_act_1x128_kernel(const uint16_t* __
     }
 }
 
+template <bool POW2>
+__global__ void __launch_bounds__(256) quant_act_1x128_kernel(const uint16_t* __restrict__ x, int64_t M, int64_t K,
+                                                              int64_t ldx, uint8_t* __restrict__ q,
+                                                              float* __restrict__ s) {
+    pdl_launch_dependents();
+    quant_act_1x128_rows<POW2>(x, M, K, ldx, q, s, blockIdx.x);
+}
+
 // ------------------------------------------------------------------ 128x128
 // One CTA (256 threads) per 128x128 block.  Thread t covers rows
 // t/16 + 16*i (i < 8) and columns 8*(t%16) .. +7 of the block: each
 // 16-thread group reads one 256-byte row segment per step.
 template <bool POW2>
-__global__ void __launch_bounds__(256) quant_weight_128x128_kernel(const uint16_t* __restrict__ w, int64_t N,
-                                                                   int64_t K, int64_t ldw, uint8_t* __restrict__ q,
-                                                                   float* __restrict__ s) {
+FP8_DEV void quant_weight_block(const uint16_t* __restrict__ w, int64_t N, int64_t K, int64_t ldw,
+                                uint8_t* __restrict__ q, float* __restrict__ s, int64_t blk) {
     __shared__ float red[8];
     const int64_t nkb = K >> 7;
-    const int64_t blk = blockIdx.x;
     const int64_t nb = blk / nkb, kb = blk - nb * nkb;
     const int t = threadIdx.x;
     const int r0 = t >> 4, c = (t & 15) * 8;
@@ -137,6 +142,37 @@ __global__ void __launch_bounds__(256) quant_weight_128x128_kernel(const uint16_
               (cvt_e4m3x2(__fmul_rn(bf16_lo(ww[3]), inv), __fmul_rn(bf16_hi(ww[3]), inv)) << 16);
         *reinterpret_cast<uint2*>(qb + (r0 + 16 * i) * K) = o;
     }
+}
+
+template <bool POW2>
+__global__ void __launch_bounds__(256) quant_weight_128x128_kernel(const uint16_t* __restrict__ w, int64_t N,
+                                                                   int64_t K, int64_t ldw, uint8_t* __restrict__ q,
+                                                                   float* __restrict__ s) {
+    pdl_launch_dependents();
+    quant_weight_block<POW2>(w, N, K, ldw, q, s, blockIdx.x);
+}
+
+// ------------------------------------------------------------------ X and W in one launch
+// The two operands of a linear layer Y = X W^T: CTAs [0, nx) quantise 8 rows
+// of X each (1x128 tiles), the rest one 128x128 block of W each.  The X CTAs,
+// about 3.5 times the work of a W block at K = 7168, come first, so the last
+// wave is made of the short ones.  Both passes read disjoint inputs and write
+// disjoint outputs; one launch lets them share the GPU without a second
+// stream, and the GEMM after it can start early (programmatic launch).
+// Capped at 80 registers (three CTAs per SM, as the weight pass alone): the
+// compiler's own choice for the joined kernel, 87, allows only two.
+template <bool POW2>
+__global__ void __launch_bounds__(256, 3) quant_act_weight_kernel(const uint16_t* __restrict__ x, int64_t M,
+                                                               int64_t ldx, uint8_t* __restrict__ qx,
+                                                               float* __restrict__ sx, int64_t nx,
+                                                               const uint16_t* __restrict__ w, int64_t N,
+                                                               int64_t ldw, uint8_t* __restrict__ qw,
+                                                               float* __restrict__ sw, int64_t K) {
+    pdl_launch_dependents();
+    if (int64_t(blockIdx.x) < nx)
+        quant_act_1x128_rows<POW2>(x, M, K, ldx, qx, sx, blockIdx.x);
+    else
+        quant_weight_block<POW2>(w, N, K, ldw, qw, sw, int64_t(blockIdx.x) - nx);
 }
 
 // ------------------------------------------------------------------ 128x1, transposed
@@ -292,5 +328,25 @@ extern "C" int fp8_quant_act_128x1(const uint16_t* x, int64_t T, int64_t H, int6
         quant_act_128x1_kernel<true><<<unsigned(blocks), 256, 0, stream>>>(x, T, H, ldx, qT, s);
     else
         quant_act_128x1_kernel<false><<<unsigned(blocks), 256, 0, stream>>>(x, T, H, ldx, qT, s);
+    return launch_status();
+}
+
+extern "C" int fp8_quant_act_weight(const uint16_t* x, int64_t M, int64_t ldx, uint8_t* qx, float* sx,
+                                    const uint16_t* w, int64_t N, int64_t ldw, uint8_t* qw, float* sw, int64_t K,
+                                    uint32_t flags, fp8_stream_t stream) {
+    if (!x || !qx || !sx || !w || !qw || !sw || M <= 0 || N <= 0 || K <= 0 || ldx < K || ldw < K ||
+        (flags & ~FP8_SCALE_POW2))
+        return FP8_ERR_ARG;
+    if (K % 128 || N % 128) return FP8_ERR_SHAPE;
+    if (!aligned16(x) || !aligned16(qx) || !aligned16(w) || !aligned16(qw) || (ldx % 8) || (ldw % 8) ||
+        (reinterpret_cast<uintptr_t>(sx) & 3u) || (reinterpret_cast<uintptr_t>(sw) & 3u))
+        return FP8_ERR_ALIGN;
+    const int64_t nx = (M + kQ1Rows - 1) / kQ1Rows;
+    const int64_t blocks = nx + (N / 128) * (K / 128);
+    if (blocks > 0x7FFFFFFFll) return FP8_ERR_SHAPE;
+    if (flags & FP8_SCALE_POW2)
+        quant_act_weight_kernel<true><<<unsigned(blocks), 256, 0, stream>>>(x, M, ldx, qx, sx, nx, w, N, ldw, qw, sw, K);
+    else
+        quant_act_weight_kernel<false><<<unsigned(blocks), 256, 0, stream>>>(x, M, ldx, qx, sx, nx, w, N, ldw, qw, sw, K);
     return launch_status();
 }

@@ -49,6 +49,7 @@ _SIGS = {
     "fp8_quant_act_1x128": [_P, _I64, _I64, _I64, _P, _P, _U32, _P],
     "fp8_quant_act_128x1": [_P, _I64, _I64, _I64, _P, _P, _U32, _P],
     "fp8_quant_weight_128x128": [_P, _I64, _I64, _I64, _P, _P, _U32, _P],
+    "fp8_quant_act_weight": [_P, _I64, _I64, _P, _P, _P, _I64, _I64, _P, _P, _I64, _U32, _P],
     "fp8_gemm_blockscaled": [_P, _P, _P, _P, _I, _P, _I, _I64, _I64, _I64, _P],
     "fp8_gemm_blockscaled_ws": [_P, _P, _P, _P, _I, _P, _I, _I64, _I64, _I64, _P, _I64, _P],
     "fp8_gemm_blockscaled_pow2": [_P, _P, _P, _P, _I, _P, _I, _I64, _I64, _I64, _P],
@@ -180,6 +181,27 @@ def fp8_quant_weight_128x128(w: torch.Tensor, q=None, s=None, flags: int = 0, st
                                                                     _ptr(s, torch.float32, "s"), flags,
                                                                     _stream(stream)))
     return q, s
+
+
+def fp8_quant_act_weight(x: torch.Tensor, w: torch.Tensor, qx=None, sx=None, qw=None, sw=None, flags: int = 0,
+                         stream=None):
+    """x bf16 [M, K], w bf16 [N, K] -> (qx, sx, qw, sw) in one launch, the same
+    results as fp8_quant_act_1x128(x) and fp8_quant_weight_128x128(w)."""
+    if x.dtype != torch.bfloat16 or w.dtype != torch.bfloat16 or not (x.is_cuda and w.is_cuda):
+        raise TypeError("x and w must be CUDA bf16 tensors")
+    M, K, ldx = _rows(x, "x")
+    N, Kw, ldw = _rows(w, "w")
+    if Kw != K:
+        raise ValueError("x and w must have the same number of columns")
+    qx = torch.empty((M, K), dtype=torch.uint8, device=x.device) if qx is None else qx
+    sx = torch.empty((K // 128, M), dtype=torch.float32, device=x.device) if sx is None else sx
+    qw = torch.empty((N, K), dtype=torch.uint8, device=w.device) if qw is None else qw
+    sw = torch.empty((N // 128, K // 128), dtype=torch.float32, device=w.device) if sw is None else sw
+    _check("fp8_quant_act_weight", lib.fp8_quant_act_weight(
+        x.data_ptr(), M, ldx, _ptr(qx, torch.uint8, "qx"), _ptr(sx, torch.float32, "sx"),
+        w.data_ptr(), N, ldw, _ptr(qw, torch.uint8, "qw"), _ptr(sw, torch.float32, "sw"), K, flags,
+        _stream(stream)))
+    return qx, sx, qw, sw
 
 
 # ---------------------------------------------------------------- GEMMs

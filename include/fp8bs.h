@@ -130,6 +130,22 @@ FP8_API int fp8_quant_weight_128x128(const uint16_t* w, int64_t N, int64_t K, in
                                      uint8_t* q, float* s, uint32_t flags, fp8_stream_t stream);
 
 /* ------------------------------------------------------------------------
+ * Both operands of a linear layer Y = X W^T quantised in one launch:
+ * exactly fp8_quant_act_1x128(x, M, K, ldx, qx, sx, ...) and
+ * fp8_quant_weight_128x128(w, N, K, ldw, qw, sw, ...) with the same flags
+ * (the same codes and scales bit for bit), the two passes sharing the GPU
+ * without a second stream.  Layouts and limits as those two calls:
+ *   x  bf16 [M][ldx], qx E4M3 [M][K], sx fp32 [K/128][M]
+ *   w  bf16 [N][ldw], qw E4M3 [N][K], sw fp32 [N/128][K/128]
+ * M >= 1, N % 128 == 0, K % 128 == 0.  The block-scaled GEMMs are launched
+ * as programmatic dependent launches, so one queued right after this call
+ * sets up while it finishes.
+ * ---------------------------------------------------------------------- */
+FP8_API int fp8_quant_act_weight(const uint16_t* x, int64_t M, int64_t ldx, uint8_t* qx, float* sx,
+                                 const uint16_t* w, int64_t N, int64_t ldw, uint8_t* qw, float* sw, int64_t K,
+                                 uint32_t flags, fp8_stream_t stream);
+
+/* ------------------------------------------------------------------------
  * SwiGLU fused with 1x128 quantisation of its output: the input of the MoE
  * down-projection (the tmdrlife.com page: that activation's scaling factors are integral
  * powers of 2, so flags = FP8_SCALE_POW2 is its natural setting; the jp-study.kr page:
@@ -166,6 +182,9 @@ FP8_API int fp8_swiglu_quant_1x128(const uint16_t* y, int64_t R, int64_t I, int6
  *       fp32 (FP8_OUT_F32)
  * M >= 1, N % 128 == 0, K % 128 == 0.  Wgrad (dW = dY^T X) is this call with
  * a = dY^T and b = X^T from fp8_quant_act_128x1, FP8_BSCALE_ROW, FP8_OUT_F32.
+ * The kernel is a programmatic dependent launch: it may start while the work
+ * before it on `stream` finishes, and touches global memory only after that
+ * work has completed (the stream order is kept).
  * ---------------------------------------------------------------------- */
 FP8_API int fp8_gemm_blockscaled(const uint8_t* a, const float* sa,
                                  const uint8_t* b, const float* sb, int b_scale_mode,

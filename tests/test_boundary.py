@@ -67,6 +67,15 @@ def test_quant_argument_errors(fb):
     assert L.fp8_quant_act_128x1(FAKE, 100, 64, 64, FAKE, FAKE, 0, None) == -2          # T % 128
     assert L.fp8_quant_act_128x1(FAKE, 128, 12, 12, FAKE, FAKE, 0, None) == -2          # H % 8
     assert L.fp8_quant_weight_128x128(FAKE, 100, 128, 128, FAKE, FAKE, 0, None) == -2   # N % 128
+    aw = L.fp8_quant_act_weight      # x, M, ldx, qx, sx, w, N, ldw, qw, sw, K, flags, stream
+    assert aw(FAKE, 4, 128, FAKE, FAKE, None, 128, 128, FAKE, FAKE, 128, 0, None) == -1     # null w
+    assert aw(FAKE, 0, 128, FAKE, FAKE, FAKE, 128, 128, FAKE, FAKE, 128, 0, None) == -1     # M = 0
+    assert aw(FAKE, 4, 128, FAKE, FAKE, FAKE, 128, 120, FAKE, FAKE, 128, 0, None) == -1     # ldw < K
+    assert aw(FAKE, 4, 128, FAKE, FAKE, FAKE, 100, 128, FAKE, FAKE, 128, 0, None) == -2     # N % 128
+    assert aw(FAKE, 4, 200, FAKE, FAKE, FAKE, 128, 200, FAKE, FAKE, 200, 0, None) == -2     # K % 128
+    assert aw(FAKE, 4, 128, FAKE, FAKE, FAKE + 8, 128, 128, FAKE, FAKE, 128, 0, None) == -3  # misaligned w
+    assert aw(FAKE, 4, 128, FAKE, FAKE, FAKE, 128, 132, FAKE, FAKE, 128, 0, None) == -3     # ldw % 8
+    assert aw(FAKE, 4, 128, FAKE, FAKE, FAKE, 128, 128, FAKE, FAKE, 128, 4, None) == -1     # unknown flag
     assert L.fp8_cast_e4m3(None, 5, FAKE, None) == -1
     assert L.fp8_cast_e4m3(None, 0, None, None) == 0                                    # empty: no-op
 

@@ -170,3 +170,37 @@ def test_quant_act_128x1_wgrad_full(fb, orc):
         qr, sr = orc.quant_act_128x1(S.bf16_bits(d[name]))
         assert_same_bits(qT, qr, name + " qT")
         assert_same_bits(s, sr, name + " s")
+
+
+@pytest.mark.parametrize("flags", [0, 1])
+def test_quant_act_weight_one_launch_dense_linear_full(fb, orc, flags):
+    """X [4096,7168] and W [7168,7168] quantised in one launch: codes and
+    scales of both bit for bit those of the oracle's 1x128 and 128x128 rules."""
+    d = S.dense_linear()
+    qx, sx, qw, sw = fb.fp8_quant_act_weight(d["x"].cuda(), d["w"].cuda(), flags=flags)
+    qxr, sxr = orc.quant_act_1x128(S.bf16_bits(d["x"]), flags)
+    qwr, swr = orc.quant_weight_128x128(S.bf16_bits(d["w"]), flags)
+    assert_same_bits(qx, qxr, "qx")
+    assert_same_bits(sx, sxr, "sx")
+    assert_same_bits(qw, qwr, "qw")
+    assert_same_bits(sw, swr, "sw")
+
+
+def test_quant_act_weight_one_launch_ragged_and_strided(fb, orc):
+    """M not a multiple of the 8 rows a CTA takes, padded row strides for both
+    operands, the edge rows of the 1x128 tests in X and a zero block in W."""
+    M, N, K = 300, 384, 640
+    x = torch.zeros((M, K + 24), dtype=torch.bfloat16)
+    x[:, :K] = _bf16((M, K), 5)
+    x[:8, :K] = _edge_tensor(8, K)
+    w = torch.zeros((N, K + 8), dtype=torch.bfloat16)
+    w[:, :K] = _bf16((N, K), 6, 0.02)
+    w[128:256, 128:256] = 0.0
+    for flags in (0, 1):
+        qx, sx, qw, sw = fb.fp8_quant_act_weight(x.cuda()[:, :K], w.cuda()[:, :K], flags=flags)
+        qxr, sxr = orc.quant_act_1x128(S.bf16_bits(x[:, :K].contiguous()), flags)
+        qwr, swr = orc.quant_weight_128x128(S.bf16_bits(w[:, :K].contiguous()), flags)
+        assert_same_bits(qx, qxr, "qx flags%d" % flags)
+        assert_same_bits(sx, sxr, "sx flags%d" % flags)
+        assert_same_bits(qw, qwr, "qw flags%d" % flags)
+        assert_same_bits(sw, swr, "sw flags%d" % flags)
