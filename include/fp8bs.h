@@ -22,7 +22,9 @@
  *     16-bit words (uint16_t), E4M3 data as bytes (uint8_t).
  *   - Work is enqueued asynchronously on `stream` (a cudaStream_t; NULL is the
  *     legacy default stream).  No call synchronises the host, except
- *     fp8_get_status.
+ *     fp8_get_status.  Stream order always holds: the block-scaled GEMMs are
+ *     programmatic dependent launches that set up while the work before them
+ *     drains, but touch memory only after it has completed.
  *   - The return value is FP8_OK (0) or a negative FP8_ERR_* code.  On an
  *     argument error (FP8_ERR_ARG, _SHAPE, _ALIGN) nothing is enqueued.
  *     FP8_ERR_CUDA means a launch failed (the CUDA error is left for
