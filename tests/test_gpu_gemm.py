@@ -234,3 +234,34 @@ def test_dgrad_dense_linear_sampled(fb, orc):
         qb, sb = orc.quant_weight_128x128(np.ascontiguousarray(wtb[kb * 128:(kb + 1) * 128]))
         ref = orc.gemm_blockscaled(qa, sa, qb, sb, 0)
         assert_gemm_close(got[:, kb * 128:(kb + 1) * 128], ref, True, orc, "dgrad col block %d" % kb)
+
+
+def test_gemm_queued_after_the_quantisers_reads_their_final_output(fb):
+    """The GEMM is a programmatic dependent launch: it may start while the
+    quantisers before it drain, and must read only their finished codes and
+    scales.  Three linear layers are queued back to back through the SAME
+    quantised buffers (quantise X_i and W_i in one launch, GEMM, next i), with
+    no host synchronisation; each output must equal, bit for bit, the same
+    layer run alone with the host synchronised before and after the GEMM."""
+    M, N, K = 1024, 2048, 3072
+    g = torch.Generator(device="cuda").manual_seed(11)
+    xs = [(torch.randn((M, K), device="cuda", generator=g) * (1 + i)).to(torch.bfloat16) for i in range(3)]
+    ws = [(torch.randn((N, K), device="cuda", generator=g) * 0.02 * (3 - i)).to(torch.bfloat16) for i in range(3)]
+    qx = torch.empty((M, K), dtype=torch.uint8, device="cuda")
+    sx = torch.empty((K // 128, M), dtype=torch.float32, device="cuda")
+    qw = torch.empty((N, K), dtype=torch.uint8, device="cuda")
+    sw = torch.empty((N // 128, K // 128), dtype=torch.float32, device="cuda")
+    ys = [torch.empty((M, N), dtype=torch.bfloat16, device="cuda") for _ in range(3)]
+    for rep in range(3):
+        torch.cuda.synchronize()
+        for i in range(3):
+            fb.fp8_quant_act_weight(xs[i], ws[i], qx, sx, qw, sw)
+            fb.fp8_gemm_blockscaled(qx, sx, qw, sw, 0, torch.bfloat16, d=ys[i])
+        torch.cuda.synchronize()
+        assert fb.fp8_get_status() == 0
+        for i in range(3):
+            fb.fp8_quant_act_weight(xs[i], ws[i], qx, sx, qw, sw)
+            torch.cuda.synchronize()
+            y_alone = fb.fp8_gemm_blockscaled(qx, sx, qw, sw, 0, torch.bfloat16)
+            torch.cuda.synchronize()
+            assert torch.equal(ys[i].view(torch.int16), y_alone.view(torch.int16)), "layer %d rep %d" % (i, rep)

@@ -186,6 +186,22 @@ def test_quant_act_weight_one_launch_dense_linear_full(fb, orc, flags):
     assert_same_bits(sw, swr, "sw")
 
 
+@pytest.mark.parametrize("M,N,K", [(1, 128, 128), (9, 128, 256), (7, 256, 1152), (8, 128, 128)])
+def test_quant_act_weight_one_launch_small_shapes(fb, orc, M, N, K):
+    """One row, one weight block, and row counts that leave the last X CTA
+    partly empty, both scale modes, against the oracle."""
+    x = _bf16((M, K), M + K, 2.0)
+    w = _bf16((N, K), N + K + 1, 0.05)
+    for flags in (0, 1):
+        qx, sx, qw, sw = fb.fp8_quant_act_weight(x.cuda(), w.cuda(), flags=flags)
+        qxr, sxr = orc.quant_act_1x128(S.bf16_bits(x), flags)
+        qwr, swr = orc.quant_weight_128x128(S.bf16_bits(w), flags)
+        assert_same_bits(qx, qxr, "qx")
+        assert_same_bits(sx, sxr, "sx")
+        assert_same_bits(qw, qwr, "qw")
+        assert_same_bits(sw, swr, "sw")
+
+
 def test_quant_act_weight_one_launch_ragged_and_strided(fb, orc):
     """M not a multiple of the 8 rows a CTA takes, padded row strides for both
     operands, the edge rows of the 1x128 tests in X and a zero block in W."""
