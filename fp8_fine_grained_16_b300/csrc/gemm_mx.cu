@@ -161,6 +161,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             tmem_relinquish();
         }
     }
+    // Launched as a programmatic dependent launch, the kernel may have started
+    // while the one before it on the stream is still running: everything
+    // above touches only this CTA's own shared memory, TMEM and the kernel
+    // parameters; from here on it reads and writes global memory.
+    pdl_wait();
+
     // grouped: the per-expert tile list (offsets and row-pair prefix in shared memory)
     int32_t* off_s = reinterpret_cast<int32_t*>(smem + L::kGrpOff);
     int32_t* pre_s = off_s + (kMaxExperts + 1);
@@ -504,23 +510,28 @@ static int launch(const CUtensorMap& ma, const CUtensorMap& mb, const Args& args
     auto kern = gemm_mx_pair_kernel<PAIR, S, BMODE, OUT_F32, GROUPED>;
     static unsigned char smem_opted_in[kMaxDevices] = {};
     if (!opt_in_dynamic_smem(kern, Lay::kDynSmem, smem_opted_in)) return FP8_ERR_CUDA;
+    // a programmatic dependent launch (the kernel waits before its first
+    // global access), as the promoted GEMMs
     cudaLaunchConfig_t cfg = {};
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = 2;
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    attr[1].id = cudaLaunchAttributeClusterDimension;
+    attr[1].val.clusterDim.x = 2;
+    attr[1].val.clusterDim.y = 1;
+    attr[1].val.clusterDim.z = 1;
     cfg.blockDim = dim3(kThreads);
     cfg.dynamicSmemBytes = Lay::kDynSmem;
     cfg.stream = stream;
+    cfg.attrs = attr;
     if constexpr (!PAIR) {
         // one CTA per SM (shared memory and launch bounds allow no more)
+        cfg.numAttrs = 1;
         cfg.gridDim = dim3(sms);
         if (cudaLaunchKernelEx(&cfg, kern, ma, mb, args) != cudaSuccess) return FP8_ERR_CUDA;
         return cudaGetLastError() == cudaSuccess ? FP8_OK : FP8_ERR_CUDA;
     }
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = 2;
     int max_clusters = 0;
     cfg.gridDim = dim3(2 * (sms / 2));
     if (cudaOccupancyMaxActiveClusters(&max_clusters, kern, &cfg) != cudaSuccess || max_clusters <= 0)

@@ -22,8 +22,8 @@
  *     16-bit words (uint16_t), E4M3 data as bytes (uint8_t).
  *   - Work is enqueued asynchronously on `stream` (a cudaStream_t; NULL is the
  *     legacy default stream).  No call synchronises the host, except
- *     fp8_get_status.  Stream order always holds: the promoted block-scaled
- *     GEMMs (fp8_gemm_blockscaled*, fp8_grouped_gemm_blockscaled) are
+ *     fp8_get_status.  Stream order always holds: the block-scaled GEMMs
+ *     (the fp8_gemm_blockscaled* and fp8_grouped_gemm_blockscaled* calls) are
  *     programmatic dependent launches that set up while the work before them
  *     drains, but touch memory only after it has completed.
  *   - The return value is FP8_OK (0) or a negative FP8_ERR_* code.  On an
@@ -140,7 +140,7 @@ FP8_API int fp8_quant_weight_128x128(const uint16_t* w, int64_t N, int64_t K, in
  * without a second stream.  Layouts and limits as those two calls:
  *   x  bf16 [M][ldx], qx E4M3 [M][K], sx fp32 [K/128][M]
  *   w  bf16 [N][ldw], qw E4M3 [N][K], sw fp32 [N/128][K/128]
- * M >= 1, N % 128 == 0, K % 128 == 0.  The promoted block-scaled GEMMs are
+ * M >= 1, N % 128 == 0, K % 128 == 0.  The block-scaled GEMMs are
  * programmatic dependent launches, so one queued right after this call sets
  * up while it finishes.
  * ---------------------------------------------------------------------- */
