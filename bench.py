@@ -866,6 +866,7 @@ def run_reference(args, ws, rank):
 
 # ---------------------------------------------------------------- single-kernel cases (for ncu)
 CASES = ("dense", "wgrad", "wgrad_small", "q8", "dgrad_transpose", "quant_1x128", "quant_1x128_h", "quant_128x1",
+         "quant_act_weight",
          "quant_128x128",
          "grouped_up_small", "grouped_down_small", "grouped_down_small_pow2", "route", "permute", "combine", "swiglu",
          "pow2_dense", "pow2_wgrad_small")
@@ -936,6 +937,11 @@ def run_case(name: str, reps: int):
         qx, sx = F.fp8_quant_act_1x128(x)
         fn = lambda: F.fp8_quant_act_1x128(x, qx, sx)
         work = "X [4096,7168]"
+    elif name == "quant_act_weight":
+        x, w = bf16(M, K), bf16(N, K)
+        qx, sx, qw, sw = F.fp8_quant_act_weight(x, w)
+        fn = lambda: F.fp8_quant_act_weight(x, w, qx, sx, qw, sw)
+        work = "X [4096,7168] and W [7168,7168], one launch"
     elif name == "quant_1x128_h":
         x = bf16(32768, 2048)
         qx, sx = F.fp8_quant_act_1x128(x)
